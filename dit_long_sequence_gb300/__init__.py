@@ -1,0 +1,16 @@
+"""GB300-native dense bidirectional long-sequence attention for DiT denoising.
+
+The compute path is libditattn.so (hand-written sm_103a CUDA behind a C ABI,
+``include/dit_attn.h``); ``binding`` is a thin ctypes layer over it.  Importing
+the package does not load the library; the first use of an operation does, and
+fails loudly if the library has not been built.
+"""
+__all__ = ["attn_fwd", "lse_merge", "qkv_to_head_major", "check_watchdog", "DitError",
+           "library_path"]
+
+
+def __getattr__(name):
+    if name in __all__:
+        from . import binding
+        return getattr(binding, name)
+    raise AttributeError(name)

@@ -1,0 +1,166 @@
+/*
+ * dit_attn.h -- C ABI of libditattn.so: dense bidirectional long-sequence
+ * attention for DiT video denoising on one NVIDIA GB300 (sm_103a).
+ *
+ * Three operations, all asynchronous on a caller-supplied CUDA stream:
+ *
+ *   dit_attn_fwd           softmax(scale * Q K^T) V plus the per-row
+ *                          log-sum-exp, Q/K/V read through arbitrary
+ *                          (b, n, h) strides, key-only padding mask.
+ *   dit_attn_lse_merge     exact combine of (O, LSE) partials computed over
+ *                          disjoint key chunks.
+ *   dit_qkv_to_head_major  split of a fused [B, N, 3, H, D] projection
+ *                          buffer into three head-major [B, H, N, D] tensors.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *   allocates no memory, copies nothing between host and device and keeps no
+ *   per-call state; per-device caches hold only kernel attributes.
+ * - Strides are in ELEMENTS, not bytes.
+ * - Argument, shape, stride and alignment checks run on the host before any
+ *   launch.  A failed check returns a non-zero status and enqueues nothing.
+ * - DIT_ERR_CUDA means a CUDA call failed while enqueueing; the CUDA error is
+ *   left for the caller to query (cudaGetLastError / cudaPeekAtLastError).
+ * - Calls are reentrant.  Input buffers must stay valid until the stream has
+ *   executed the call; outputs are valid once the stream has passed it.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ * - Every spin-wait inside the kernels is bounded (about two seconds).  A wait
+ *   that runs out records DIT_ERR_TIMEOUT in a device status word, the kernel
+ *   winds down without faulting, and dit_check_watchdog() reports it.
+ */
+#ifndef DIT_ATTN_H
+#define DIT_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *dit_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    DIT_OK = 0,
+    DIT_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad scale, ... */
+    DIT_ERR_UNSUPPORTED = 2, /* a legal request outside what is built (e.g. D) */
+    DIT_ERR_ALIGNMENT = 3,   /* a pointer or stride breaks the 16-byte rules  */
+    DIT_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed           */
+    DIT_ERR_TIMEOUT = 5      /* a bounded in-kernel wait ran out (watchdog)   */
+} dit_status_t;
+
+typedef enum { DIT_BF16 = 0, DIT_F32 = 1 } dit_dtype_t;
+
+/* Element strides of a [B, N, H, D] view. */
+typedef struct {
+    int64_t b, n, h, d;
+} dit_strides4_t;
+
+typedef struct {
+    dit_strides4_t q, k, v, o;
+} dit_attn_strides_t;
+
+/*
+ * dit_attn_fwd -- O = softmax(scale * Q K^T) V and LSE = ln sum_j exp(scale q.k_j)
+ *
+ * Defined by "Scaling Video Generation Across NVL72 rack with TensorRT-LLM":
+ * section "The Scaling Challenge in Video Generation" (dense, unmasked,
+ * bidirectional attention over the full N x N block, every denoising step)
+ * and section "Attention2D Parallelism", paragraph "Local Attention" (the
+ * inner backend returns the output [B,S,H,D] and an LSE [B,H,S] recording the
+ * softmax normaliser, so partial passes over key chunks merge exactly).  The
+ * key mask follows "8 卡怎么分 token：LTX-2 序列并行的 all2all 到底搬了什么",
+ * "数据流拆解" / "构造 padding mask": a key-only mask, pads at the tail, pad
+ * query rows attend all valid keys.  Strided Q/K/V follow "CUDA IPC
+ * Ulysses：在 H100 上重叠 Attention 通信", "基线与瓶颈": V of a fused QKV
+ * projection is read as a strided view with no packing copy.
+ *
+ * q      bf16, element (b, i, h, d) at q + b*s.q.b + i*s.q.n + h*s.q.h + d, i < Nq
+ * k, v   bf16, same form with s.k / s.v, j < Nkv
+ * strides  s.q.d, s.k.d, s.v.d, s.o.d must be 1.  The b, n, h strides of q/k/v
+ *          must be positive multiples of 8 elements (16 bytes); those of o
+ *          multiples of 16 bytes of out_dtype.  Base pointers 16-byte aligned.
+ * B, Nq, Nkv, H  >= 0 (a zero size is a no-op); D in {64, 128}.
+ * key_valid_len  keys j >= key_valid_len are masked out; 0 <= key_valid_len <= Nkv.
+ *          Masked keys are never read, so pad rows may hold any bits.
+ *          key_valid_len == 0 yields O = 0 and LSE = -inf for every row.
+ * scale  finite and > 0 (typically 1/sqrt(D)).
+ * out    O, out_dtype DIT_F32 or DIT_BF16, addressed with s.o ([B, Nq, H, D]).
+ * lse    fp32 [B, H, Nq] contiguous, natural log, includes `scale`.
+ * Returns DIT_OK once enqueued.
+ */
+dit_status_t dit_attn_fwd(const void *q, const void *k, const void *v,
+                          const dit_attn_strides_t *strides,
+                          int B, int Nq, int Nkv, int H, int D,
+                          int key_valid_len, float scale,
+                          void *out, dit_dtype_t out_dtype, float *lse,
+                          dit_stream_t stream);
+
+/*
+ * dit_attn_lse_merge -- combine n_chunks partial (O_k, LSE_k) computed for the
+ * same queries over disjoint key spans into the single-pass result.
+ *
+ * Defined by "Scaling Video Generation Across NVL72 rack with TensorRT-LLM",
+ * "Attention2D Parallelism", paragraph "Merge phase" (one batched combine of
+ * the col_size received (output, LSE) pairs) and "Ring Attention", paragraph
+ * "Online-softmax merge" (fp32 merge until the result equals one global pass):
+ *   M = max_k LSE_k,  w_k = exp(LSE_k - M),  O = sum_k w_k O_k / sum_k w_k,
+ *   LSE = M + ln sum_k w_k.  Chunks with LSE_k = -inf get weight 0 (their O_k
+ *   is not read); a row whose chunks are all -inf yields O = 0, LSE = -inf.
+ *
+ * o_parts    fp32, chunk k row (b, i, h) at o_parts + k*o_chunk_stride +
+ *            ((b*Nq + i)*H + h)*D  (each chunk a contiguous [B, Nq, H, D]).
+ * lse_parts  fp32, chunk k at lse_parts + k*lse_chunk_stride, [B, H, Nq] contiguous.
+ * n_chunks in [1, 64]; D in {64, 128}.  o_chunk_stride a multiple of 4 elements.
+ * out        [B, Nq, H, D] contiguous, out_dtype DIT_F32 or DIT_BF16.
+ * lse_out    fp32 [B, H, Nq] contiguous, may be NULL.
+ * All pointers 16-byte aligned.  Output must not overlap any input.
+ */
+dit_status_t dit_attn_lse_merge(const float *o_parts, int64_t o_chunk_stride,
+                                const float *lse_parts, int64_t lse_chunk_stride,
+                                int n_chunks, int B, int Nq, int H, int D,
+                                void *out, dit_dtype_t out_dtype, float *lse_out,
+                                dit_stream_t stream);
+
+/*
+ * dit_qkv_to_head_major -- bit-exact split/permute of a fused QKV projection.
+ *
+ * Defined by "Scaling Video Generation Across NVL72 rack with TensorRT-LLM",
+ * "Ulysses Parallelism" (the swap from sequence-major [B,S,H,D] to the
+ * head-sharded layout before attention; paragraph "Fused vs. unfused QKV
+ * all-to-all": the stacked buffer is [B, S, 3, H, D]) and "CUDA IPC
+ * Ulysses：在 H100 上重叠 Attention 通信", "Strided Copy Engine scatter"
+ * (the source pitch comes straight from the input stride; head and channel
+ * must be contiguous within each sequence row).
+ *
+ * qkv     bf16; element (b, n, t, h, d) at qkv + b*stride_b + n*stride_n +
+ *         (t*H + h)*D + d, t = 0 (q), 1 (k), 2 (v).  stride_b, stride_n
+ *         multiples of 8 elements; base 16-byte aligned; D a multiple of 8.
+ * q_out, k_out, v_out  each [B, H, N, D] contiguous bf16, 16-byte aligned:
+ *         out_t[((b*H + h)*N + n)*D + d] = qkv(b, n, t, h, d).
+ */
+dit_status_t dit_qkv_to_head_major(const void *qkv, int64_t stride_b, int64_t stride_n,
+                                   int B, int N, int H, int D,
+                                   void *q_out, void *k_out, void *v_out,
+                                   dit_stream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *dit_status_string(dit_status_t s);
+
+/*
+ * dit_check_watchdog -- synchronise `stream`, read and clear the device
+ * status word of the current device.  Returns DIT_OK, DIT_ERR_TIMEOUT (a
+ * bounded in-kernel wait ran out; `info`, if non-NULL, receives four words:
+ * code, block index, warp role, wait site) or DIT_ERR_CUDA.
+ */
+dit_status_t dit_check_watchdog(dit_stream_t stream, uint32_t info[4]);
+
+/* Library version, (major << 16) | minor. */
+uint32_t dit_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIT_ATTN_H */

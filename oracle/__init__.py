@@ -1,0 +1,212 @@
+"""Plain fp64 CPU oracle for the attention / LSE-merge / QKV-layout path.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this package.  The product path (the CUDA library
+and its Python binding) never imports, links or runs anything here, and this
+package never imports the product path: the two share no code.
+
+Contents
+--------
+``attn``                 dense bidirectional attention + LSE, fp64, in C
+                         (``attn_oracle.c``), on whole heads or on sampled rows.
+``lse_merge``            batched (O, LSE) combine, fp64, numpy.
+``lse_merge_streaming``  the same combine as a streaming pairwise recurrence.
+``qkv_to_head_major``    the fused-QKV split/permute, numpy indexing.
+
+Citations (page title, section):
+  * "Scaling Video Generation Across NVL72 rack with TensorRT-LLM":
+    - "The Scaling Challenge in Video Generation": dense, unmasked,
+      bidirectional N x N attention every step.
+    - "Ring Attention", paragraph "Online-softmax merge": each partial pass
+      yields an output and an LSE; they are merged in fp32 by a streaming
+      softmax recurrence until the result equals one global pass.
+    - "Attention2D Parallelism", paragraphs "Local Attention" and "Merge phase":
+      partial O is [B,S,H,D], LSE is [B,H,S]; a batched combine merges the
+      col_size partials over disjoint key spans; the "Difference from Ring"
+      table names Ring's recurrence the sigmoid / logsigmoid form.
+    - "Ulysses Parallelism", paragraph "Fused vs. unfused QKV all-to-all":
+      the stacked buffer is [B, S, 3, H, D].
+  * "8 卡怎么分 token：LTX-2 序列并行的 all2all 到底搬了什么", "数据流拆解",
+    paragraph "构造 padding mask": key-only (1,1,T) mask, pads at the tail.
+  * "CUDA IPC Ulysses：在 H100 上重叠 Attention 通信", "基线与瓶颈": V of a fused
+    QKV projection is a legal strided view; no packing copy.
+
+Parity status: every function here is pinned by the CPU tests (brute force,
+closed forms, library special cases and invariants); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (plain -O2, IEEE fp64, OpenMP)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fno-fast-math", "-fopenmp", "-shared", "-fPIC",
+           "-std=c11", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def bind_library(path: str):
+    """ctypes handle for a compiled oracle library at ``path``."""
+    lib = ctypes.CDLL(path)
+    f = lib.oracle_attn_head_rows
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
+                  ctypes.POINTER(ctypes.c_int64),
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_double, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_int]
+    lib.oracle_max_threads.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = bind_library(_LIB_PATH)
+    return _lib
+
+
+def max_threads() -> int:
+    """OpenMP threads the C oracle runs with."""
+    return int(_load().oracle_max_threads())
+
+
+def _bf16_view_strides(a: np.ndarray, name: str):
+    """Element strides (b, n, h) of a [B, N, H, D] uint16 view with d contiguous."""
+    if a.dtype != np.uint16 or a.ndim != 4:
+        raise TypeError(f"{name}: expected a 4-D uint16 array of bf16 bits, got {a.dtype} {a.shape}")
+    st = [s // 2 for s in a.strides]
+    if any(s % 2 for s in a.strides) or (a.shape[3] > 1 and st[3] != 1):
+        raise ValueError(f"{name}: the head dimension must be contiguous")
+    return (ctypes.c_int64 * 3)(st[0], st[1], st[2])
+
+
+def attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, key_valid_len: int | None = None,
+         scale: float | None = None, rows: np.ndarray | None = None, threads: int = 0,
+         lib=None):
+    """fp64 attention with LSE on bf16 inputs given as uint16 bit arrays.
+
+    q: [B, Nq, H, D], k/v: [B, Nkv, H, D] -- any numpy views (strided views
+    of a fused buffer included) whose last axis is contiguous.
+
+    rows None  -> every query row; returns O [B, Nq, H, D], LSE [B, H, Nq].
+    rows given -> an int array [B, H, R] of query rows per head; returns
+                  O [B, H, R, D] and LSE [B, H, R] for those rows.
+    Keys j >= key_valid_len are masked (default: none).  ``lib`` selects another
+    compiled copy of the oracle (the mutation tests use it).
+    """
+    lib = _load() if lib is None else lib
+    B, Nq, H, D = q.shape
+    Nkv = k.shape[1]
+    if k.shape != (B, Nkv, H, D) or v.shape != (B, Nkv, H, D):
+        raise ValueError("k and v must be [B, Nkv, H, D] with q's B, H, D")
+    kvl = Nkv if key_valid_len is None else int(key_valid_len)
+    sc = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    qs, ks, vs = _bf16_view_strides(q, "q"), _bf16_view_strides(k, "k"), _bf16_view_strides(v, "v")
+    full = rows is None
+    if full:
+        rows = np.broadcast_to(np.arange(Nq, dtype=np.int32), (B, H, Nq))
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    R = rows.shape[2]
+    o = np.empty((B, H, R, D), dtype=np.float64)
+    lse = np.empty((B, H, R), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            r_bh = np.ascontiguousarray(rows[b, h])
+            o_bh = np.empty((R, D), dtype=np.float64)
+            l_bh = np.empty((R,), dtype=np.float64)
+            rc = lib.oracle_attn_head_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, qs, ks, vs,
+                                           Nq, Nkv, D, kvl, sc, b, h, r_bh.ctypes.data, R,
+                                           o_bh.ctypes.data, l_bh.ctypes.data, int(threads))
+            if rc != 0:
+                raise ValueError(f"oracle_attn_head_rows failed with {rc}")
+            o[b, h] = o_bh
+            lse[b, h] = l_bh
+    if full:
+        return np.ascontiguousarray(o.transpose(0, 2, 1, 3)), lse
+    return o, lse
+
+
+def lse_merge(o_parts: np.ndarray, lse_parts: np.ndarray):
+    """Batched combine of n partial passes over disjoint key spans (fp64).
+
+    o_parts [n, B, S, H, D], lse_parts [n, B, H, S] -> O [B, S, H, D], LSE [B, H, S].
+    With M = max_k L_k and w_k = exp(L_k - M):  O = sum_k w_k O_k / sum_k w_k,
+    LSE = M + ln sum_k w_k.  A chunk with L_k = -inf has weight 0; if every
+    chunk is -inf the row is O = 0, LSE = -inf.
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    M = lse_parts.max(axis=0)                                   # [B,H,S]
+    empty = np.isneginf(M)
+    Ms = np.where(empty, 0.0, M)
+    w = np.exp(lse_parts - Ms[None])                            # [n,B,H,S], 0 for -inf
+    lam = w.sum(axis=0)                                         # [B,H,S]
+    wt = np.transpose(w, (0, 1, 3, 2))[..., None]               # [n,B,S,H,1]
+    num = (wt * np.where(wt > 0, o_parts, 0.0)).sum(axis=0)     # [B,S,H,D]
+    lam_t = np.transpose(lam, (0, 2, 1))[..., None]
+    o = np.where(lam_t > 0, num / np.where(lam_t > 0, lam_t, 1.0), 0.0)
+    lse = np.where(empty, -np.inf, Ms + np.log(np.where(empty, 1.0, lam)))
+    return o, lse
+
+
+def lse_merge_streaming(o_parts: np.ndarray, lse_parts: np.ndarray):
+    """Ring's streaming form of the same combine, one partial at a time (fp64).
+
+    Running (O, L) absorbs (O_b, L_b) by
+        O <- O - sigmoid(L_b - L) * (O - O_b)
+        L <- L - log sigmoid(L - L_b)
+    The sigmoid weight is evaluated as exp(L_b - L_new) with
+    L_new = logaddexp(L, L_b); an all -inf pair leaves the state unchanged.
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    O = np.zeros(o_parts.shape[1:], dtype=np.float64)
+    L = np.full(lse_parts.shape[1:], -np.inf)
+    for kk in range(o_parts.shape[0]):
+        Lb = lse_parts[kk]
+        Ob = o_parts[kk]
+        both_empty = np.isneginf(L) & np.isneginf(Lb)
+        with np.errstate(invalid="ignore"):
+            Lnew = np.where(both_empty, -np.inf, np.logaddexp(L, Lb))
+            sig = np.where(both_empty, 0.0, np.exp(Lb - np.where(both_empty, 0.0, Lnew)))
+        sig_t = np.transpose(sig, (0, 2, 1))[..., None]
+        Obs = np.where(sig_t > 0, Ob, 0.0)
+        O = O - sig_t * (O - Obs)
+        L = Lnew
+    return O, L
+
+
+def qkv_to_head_major(qkv: np.ndarray):
+    """Split a fused [B, N, 3, H, D] buffer into three [B, H, N, D] arrays.
+
+    out_t[b, h, n, d] = qkv[b, n, t, h, d] for t in (q, k, v): a pure copy.
+    """
+    if qkv.ndim != 5 or qkv.shape[2] != 3:
+        raise ValueError("expected a [B, N, 3, H, D] array")
+    return tuple(np.ascontiguousarray(qkv[:, :, t].transpose(0, 2, 1, 3)) for t in range(3))
