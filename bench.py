@@ -1,0 +1,494 @@
+"""Benchmark: attention TFLOP/s (4*B*H*Nq*Nkv*D) on one GB300, and its
+fraction of the measured dense-bf16 peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one pass of the hot path over one batch of synthetic input.  For the
+default workload (ltx2_padded: B=1, H=32, D=128, 24,200 valid tokens padded to
+24,576, key-only mask) the step is: split the fused [B, T, 3, H, D] QKV
+projection into head-major Q/K/V (dit_qkv_to_head_major), then attention with
+LSE over the head-major views (dit_attn_fwd).  Other workloads: cosmos3_nano
+(attention straight on strided views of the fused buffer), wan22_a14b
+(separate Q/K/V), ring9 (9 key chunks, 9 attention calls + dit_attn_lse_merge).
+
+Printed (rank 0, one JSON line): value = algorithmic FLOPs of all ranks / max
+over ranks of the device time of K steps; e2e = the same metric through the
+C ABI with the step's inputs copied from pinned host memory and O + LSE copied
+back inside the timed region; roofline = the attention kernel timed with CUDA
+events on its own stream inside the timed region; cpu_baseline = the fp64
+oracle on a bounded row sample on the host cores.  Inputs exceed the 129 MB
+L2, so no flush runs between steps.  N > 1 runs independent replicas (weak
+scaling); the path has no cross-GPU exchange.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s (4*B*H*Nq*Nkv*D) and % of GB300 dense BF16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------- helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for fn in ("attn_fwd.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "dit_long_sequence_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """dram bytes per attention launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", f"attn_fwd_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    text = open(p, encoding="utf-8").read()
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    """torchrun environment -> (rank, world, local_rank); N = 1 needs no process group."""
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE={world}")
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def reduce_max(value: float) -> float:
+    """Max over ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------------- the step
+
+class Step:
+    """Device buffers and the launch sequence of one step for a workload."""
+
+    def __init__(self, w, dev):
+        import torch
+        import dit_long_sequence_gb300 as dl
+        from dit_long_sequence_gb300 import workloads as wl
+        self.w, self.dev, self.dl = w, dev, dl
+        self.stream = torch.cuda.current_stream(dev)
+        B, N, H, D = w.B, w.N, w.H, w.D
+        self.mode = "layout+attn" if w.name in ("ltx2_padded", "tiny") else (
+            "chunked+merge" if w.kv_chunks > 1 else "attn")
+        if self.mode == "layout+attn" or w.fused:
+            self.fused = wl.randn_bf16((B, N, 3, H, D), w.seed, dev)
+            self.q = self.k = self.v = None
+            if self.mode == "layout+attn":
+                self.planes = tuple(torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev) for _ in range(3))
+                self.q, self.k, self.v = (p.permute(0, 2, 1, 3) for p in self.planes)   # [B,N,H,D] views
+            else:
+                self.q, self.k, self.v = self.fused[:, :, 0], self.fused[:, :, 1], self.fused[:, :, 2]
+        else:
+            self.fused = None
+            self.q, self.k, self.v, _ = wl.make_qkv(B, N, H, D, w.seed, device=dev)
+        self.out = torch.empty((B, N, H, D), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        if self.mode == "chunked+merge":
+            n = w.kv_chunks
+            self.o_parts = torch.empty((n, B, N, H, D), dtype=torch.float32, device=dev)
+            self.l_parts = torch.empty((n, B, H, N), dtype=torch.float32, device=dev)
+        self.launches_per_step = {"layout+attn": 2, "attn": 1, "chunked+merge": w.kv_chunks + 1}[self.mode]
+        self.attn_events = []
+
+    def input_tensor(self):
+        """The tensor a user uploads per step (for the e2e leg)."""
+        if self.fused is not None:
+            return self.fused
+        return None
+
+    def run(self, record=False):
+        import torch
+        dl, w = self.dl, self.w
+        ev = None
+        if self.mode == "layout+attn":
+            dl.qkv_to_head_major(self.fused, outs=self.planes, stream=self.stream)
+            if record:
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ev[0].record(self.stream)
+            dl.attn_fwd(self.q, self.k, self.v, key_valid_len=w.key_valid_len, out=self.out, lse=self.lse,
+                        stream=self.stream)
+            if record:
+                ev[1].record(self.stream)
+                self.attn_events.append(ev)
+        elif self.mode == "attn":
+            if record:
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ev[0].record(self.stream)
+            dl.attn_fwd(self.q, self.k, self.v, key_valid_len=w.key_valid_len, out=self.out, lse=self.lse,
+                        stream=self.stream)
+            if record:
+                ev[1].record(self.stream)
+                self.attn_events.append(ev)
+        else:
+            n = w.kv_chunks
+            cl = w.N // n
+            if record:
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ev[0].record(self.stream)
+            for c in range(n):
+                dl.attn_fwd(self.q, self.k[:, c * cl:(c + 1) * cl], self.v[:, c * cl:(c + 1) * cl],
+                            out=self.o_parts[c], lse=self.l_parts[c], stream=self.stream)
+            if record:
+                ev[1].record(self.stream)
+                self.attn_events.append(ev)
+            dl.lse_merge(self.o_parts, self.l_parts, out=self.out, lse_out=self.lse, stream=self.stream)
+
+    def attn_ms_per_launch(self):
+        import torch
+        torch.cuda.synchronize()
+        times = [a.elapsed_time(b) for a, b in self.attn_events]
+        per = self.w.kv_chunks if self.mode == "chunked+merge" else 1
+        return statistics.mean(times) / per if times else float("nan")
+
+
+def time_merge_kernel(dev, B, N, H, D, n_chunks=9, reps=5):
+    """HBM roofline of dit_attn_lse_merge on ring-style partials of this shape."""
+    import torch
+    import dit_long_sequence_gb300 as dl
+    from dit_long_sequence_gb300 import workloads as wl
+    g = wl.generator(dev, 77)
+    o = torch.randn((n_chunks, B, N, H, D), generator=g, device=dev)
+    l = torch.randn((n_chunks, B, H, N), generator=g, device=dev) + 10.0
+    out = torch.empty((B, N, H, D), device=dev)
+    lo = torch.empty((B, H, N), device=dev)
+    for _ in range(3):
+        dl.lse_merge(o, l, out=out, lse_out=lo)
+    s = torch.cuda.current_stream(dev)
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        dl.lse_merge(o, l, out=out, lse_out=lo)
+        b.record(s)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    nbytes = (n_chunks + 1) * (B * N * H * D * 4 + B * H * N * 4)
+    ms = statistics.median(ts)
+    del o, l, out, lo
+    return nbytes, ms
+
+
+def time_layout_kernel(step, reps=5):
+    import torch
+    if step.mode != "layout+attn":
+        return None
+    s = step.stream
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        step.dl.qkv_to_head_major(step.fused, outs=step.planes, stream=s)
+        b.record(s)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    nbytes = 2 * step.fused.numel() * 2
+    return nbytes, statistics.median(ts)
+
+
+# --------------------------------------------------------------- cpu baseline
+
+def cpu_baseline(w, dev_inputs=None, target_s=12.0):
+    """The fp64 oracle as it stands, on a bounded sample of query rows of the
+    workload (all keys), on the host cores.  Returns a dict in the metric's unit."""
+    import numpy as np
+    import oracle
+    from dit_long_sequence_gb300 import workloads as wl
+    if dev_inputs is None:
+        q, k, v, _ = wl.make_workload_inputs(w, device="cpu")
+    else:
+        q, k, v = dev_inputs
+    qb, kb, vb = wl.host_bf16_bits(q), wl.host_bf16_bits(k), wl.host_bf16_bits(v)
+    kvl = w.key_valid_len
+    per_row = 4.0 * w.kv_len * w.D
+
+    def run(rows_per_head, heads):
+        rows = wl.sample_rows(1, heads, w.N, rows_per_head, seed=w.seed)
+        qs, ks, vs = qb[:1, :, :heads], kb[:1, :, :heads], vb[:1, :, :heads]
+        t0 = time.perf_counter()
+        oracle.attn(qs, ks, vs, key_valid_len=kvl, rows=rows)
+        return time.perf_counter() - t0, rows.size
+
+    heads = min(w.H, 8)
+    t, n = run(4, heads)
+    rate = n / max(t, 1e-6)
+    rows_per_head = int(max(4, min(w.N, target_s * rate / heads)))
+    t, n = run(rows_per_head, heads)
+    tflops = n * per_row / t / 1e12
+    return {"value": tflops, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{n} query rows ({rows_per_head} per head, heads 0-{heads - 1} of batch 0) "
+                      f"x all {w.kv_len} valid keys, fp64, {t:.1f} s",
+            "rows_per_s": n / t, "seconds": t,
+            "extrapolated_full_step_s": (w.flops() / per_row) / (n / t)}
+
+
+# ------------------------------------------------------------------------ main
+
+def run_reference(args, w):
+    rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    from dit_long_sequence_gb300 import workloads as wl
+    q, k, v, _ = wl.make_workload_inputs(w, device="cpu")
+    for _ in range(args.warmup):
+        cpu_baseline(w, (q, k, v), target_s=1.0)
+    vals = [cpu_baseline(w, (q, k, v), target_s=max(2.0, 60.0 / max(args.steps, 1))) for _ in range(args.steps)]
+    value = statistics.mean(v_["value"] for v_ in vals)
+    secs = sum(v_["seconds"] for v_ in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded bf16 N(0,1))",
+            "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": vals[-1]["cores"], "kind": "oracle",
+                             "sample": vals[-1]["sample"] + " per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "D": w.D, "seq_len": w.N,
+            "key_valid_len": w.kv_len, "kv_chunks": w.kv_chunks, "fused_qkv": w.fused,
+            "out_dtype": "fp32", "global_batch": w.B, "l2": "inputs larger than the 129 MB L2, no flush",
+            "description": w.description}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="ltx2_padded")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    from dit_long_sequence_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import dit_long_sequence_gb300 as dl
+
+    step = Step(w, dev)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    rc, info = dl.check_watchdog()
+    if rc != 0:
+        raise RuntimeError(f"watchdog: {rc} {info}")
+
+    # ---------------- device-timed region
+    step.attn_events.clear()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        start.record(step.stream)
+        for _ in range(args.steps):
+            step.run(record=True)
+        stop.record(step.stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = start.elapsed_time(stop)
+    ms_total = reduce_max(ms_total)
+    ms_per_step = ms_total / args.steps
+    flops_step = w.flops()
+    value = world * flops_step * args.steps / (ms_total * 1e-3) / 1e12
+    attn_ms = step.attn_ms_per_launch()
+    per_launch_flops = flops_step / (w.kv_chunks if w.kv_chunks > 1 else 1)
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = per_launch_flops / (attn_ms * 1e-3) / 1e12
+    traffic = profiled_traffic(w.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "kernel": "attn_fwd_kernel<128,false>", "peak_kind": f"{peak_kind} dense bf16 burst",
+                "flops_per_launch": per_launch_flops, "ms_per_launch": attn_ms}
+
+    # ---------------- secondary HBM-bound kernels
+    extra = {}
+    lay = time_layout_kernel(step)
+    if lay is not None:
+        gbs = lay[0] / (lay[1] * 1e-3) / 1e9
+        extra["layout"] = {"bytes": lay[0], "ms": lay[1], "GB/s": gbs, "frac_hbm": gbs / float(peaks["hbm_gbs"])}
+    mb, mms = time_merge_kernel(dev, w.B, w.N, w.H, w.D, n_chunks=9)
+    mgbs = mb / (mms * 1e-3) / 1e9
+    extra["merge_n9"] = {"bytes": mb, "ms": mms, "GB/s": mgbs, "frac_hbm": mgbs / float(peaks["hbm_gbs"])}
+
+    # ---------------- end-to-end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(step, args, world)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded bf16 N(0,1), no weights)",
+            "config": config_of(w), "roofline": roofline, "clocks": clk.summary(),
+            "gpu_launches": step.launches_per_step * args.steps, "e2e": e2e, "kernels": extra,
+            "pct_of_bf16_peak": 100.0 * value / world / peak}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
+def run_e2e(step, args, world):
+    """Same metric through the C ABI with host buffers: per step, copy the inputs
+    from pinned host memory, run the step, copy O and LSE back."""
+    import torch
+    src = step.input_tensor()
+    if src is not None:
+        host_in = [torch.empty(src.shape, dtype=src.dtype, pin_memory=True)]
+        dev_in = [src]
+    else:
+        host_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (step.q, step.k, step.v)]
+        dev_in = [step.q, step.k, step.v]
+    for h, d in zip(host_in, dev_in):
+        h.copy_(d)
+    host_o = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
+    host_l = torch.empty(step.lse.shape, dtype=step.lse.dtype, pin_memory=True)
+    s = step.stream
+
+    def one():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        step.run()
+        host_o.copy_(step.out, non_blocking=True)
+        host_l.copy_(step.lse, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(args.steps):
+        one()
+    b.record(s)
+    torch.cuda.synchronize()
+    barrier()
+    ms = reduce_max(a.elapsed_time(b))
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = host_o.numel() * host_o.element_size() + host_l.numel() * host_l.element_size()
+    return {"value": world * step.w.flops() * args.steps / (ms * 1e-3) / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,166 @@
+"""ctypes binding of libditattn.so (include/dit_attn.h).
+
+Argument marshalling only: tensors are passed as device pointers with their
+element strides and the current CUDA stream; every step of the computation
+runs in the library's kernels.  PyTorch supplies device memory and streams.
+There is no fallback: if the library is missing or a call fails, an exception
+is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+library_path = _LIB_PATH
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"libditattn.so not found at {_LIB_PATH}; build it first with "
+        "`python -m dit_long_sequence_gb300.build` (or __graft_entry__.build())")
+
+_lib = ctypes.CDLL(_LIB_PATH)
+
+DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_ALIGNMENT, DIT_ERR_CUDA, DIT_ERR_TIMEOUT = range(6)
+DIT_BF16, DIT_F32 = 0, 1
+
+
+class Strides4(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int64), ("n", ctypes.c_int64), ("h", ctypes.c_int64), ("d", ctypes.c_int64)]
+
+
+class AttnStrides(ctypes.Structure):
+    _fields_ = [("q", Strides4), ("k", Strides4), ("v", Strides4), ("o", Strides4)]
+
+
+_vp, _i, _i64, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+
+_lib.dit_attn_fwd.restype = _i
+_lib.dit_attn_fwd.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
+                              _vp, _i, _vp, _vp]
+_lib.dit_attn_lse_merge.restype = _i
+_lib.dit_attn_lse_merge.argtypes = [_vp, _i64, _vp, _i64, _i, _i, _i, _i, _i, _vp, _i, _vp, _vp]
+_lib.dit_qkv_to_head_major.restype = _i
+_lib.dit_qkv_to_head_major.argtypes = [_vp, _i64, _i64, _i, _i, _i, _i, _vp, _vp, _vp, _vp]
+_lib.dit_status_string.restype = ctypes.c_char_p
+_lib.dit_status_string.argtypes = [_i]
+_lib.dit_check_watchdog.restype = _i
+_lib.dit_check_watchdog.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
+_lib.dit_version.restype = ctypes.c_uint32
+
+EXPORTS = ("dit_attn_fwd", "dit_attn_lse_merge", "dit_qkv_to_head_major", "dit_status_string",
+           "dit_check_watchdog", "dit_version")
+
+
+class DitError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_lib.dit_status_string(status).decode()}")
+
+
+def _check(status: int, where: str):
+    if status != DIT_OK:
+        raise DitError(status, where)
+
+
+def raw():
+    """The ctypes library handle (for callers that marshal pointers themselves)."""
+    return _lib
+
+
+def _stream_ptr(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _strides4(t: torch.Tensor) -> Strides4:
+    return Strides4(*t.stride())
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, key_valid_len: int | None = None,
+             scale: float | None = None, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+             out_dtype: torch.dtype = torch.float32, stream=None):
+    """O = softmax(scale Q K^T) V and LSE, through `dit_attn_fwd`.
+
+    q [B, Nq, H, D], k/v [B, Nkv, H, D]: bf16 CUDA tensors with any strides whose
+    last dimension is contiguous (strided views of a fused QKV buffer work as is).
+    Returns (out [B, Nq, H, D] in out_dtype, lse [B, H, Nq] fp32).
+    """
+    B, Nq, H, D = q.shape
+    Nkv = k.shape[1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a bf16 CUDA tensor")
+    if k.shape != (B, Nkv, H, D) or v.shape != (B, Nkv, H, D):
+        raise ValueError("k and v must be [B, Nkv, H, D] matching q")
+    kvl = Nkv if key_valid_len is None else int(key_valid_len)
+    sc = float(D) ** -0.5 if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, Nq, H, D), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if out.dtype not in (torch.float32, torch.bfloat16) or tuple(out.shape) != (B, Nq, H, D):
+        raise ValueError("out must be a [B, Nq, H, D] fp32 or bf16 tensor")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
+    st = AttnStrides(_strides4(q), _strides4(k), _strides4(v), _strides4(out))
+    rc = _lib.dit_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(st), B, Nq, Nkv, H, D, kvl,
+                           sc, out.data_ptr(), DIT_F32 if out.dtype == torch.float32 else DIT_BF16,
+                           lse.data_ptr(), _stream_ptr(stream))
+    _check(rc, "dit_attn_fwd")
+    return out, lse
+
+
+def lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, *, out: torch.Tensor | None = None,
+              lse_out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32, stream=None):
+    """Merge n partials: o_parts [n, B, Nq, H, D] fp32, lse_parts [n, B, H, Nq] fp32
+    (each chunk contiguous; chunks may be strided).  Returns (out, lse_out)."""
+    n, B, Nq, H, D = o_parts.shape
+    if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
+        raise TypeError("partials must be fp32")
+    if tuple(lse_parts.shape) != (n, B, H, Nq):
+        raise ValueError("lse_parts must be [n, B, H, Nq]")
+    if not o_parts[0].is_contiguous() or not lse_parts[0].is_contiguous():
+        raise ValueError("each chunk must be contiguous")
+    if out is None:
+        out = torch.empty((B, Nq, H, D), dtype=out_dtype, device=o_parts.device)
+    if lse_out is None:
+        lse_out = torch.empty((B, H, Nq), dtype=torch.float32, device=o_parts.device)
+    if not out.is_contiguous() or not lse_out.is_contiguous():
+        raise ValueError("outputs must be contiguous")
+    rc = _lib.dit_attn_lse_merge(o_parts.data_ptr(), o_parts.stride(0), lse_parts.data_ptr(), lse_parts.stride(0),
+                                 n, B, Nq, H, D, out.data_ptr(),
+                                 DIT_F32 if out.dtype == torch.float32 else DIT_BF16, lse_out.data_ptr(),
+                                 _stream_ptr(stream))
+    _check(rc, "dit_attn_lse_merge")
+    return out, lse_out
+
+
+def qkv_to_head_major(qkv: torch.Tensor, *, outs=None, stream=None):
+    """Split a fused [B, N, 3, H, D] bf16 buffer (b and n strides free, inner
+    [3, H, D] contiguous) into three contiguous [B, H, N, D] tensors."""
+    B, N, three, H, D = qkv.shape
+    if three != 3 or qkv.dtype != torch.bfloat16:
+        raise ValueError("expected a bf16 [B, N, 3, H, D] tensor")
+    if qkv.stride(4) != 1 or qkv.stride(3) != D or qkv.stride(2) != H * D:
+        raise ValueError("the [3, H, D] block of every sequence row must be contiguous")
+    if outs is None:
+        outs = tuple(torch.empty((B, H, N, D), dtype=torch.bfloat16, device=qkv.device) for _ in range(3))
+    for o in outs:
+        if not o.is_contiguous() or tuple(o.shape) != (B, H, N, D):
+            raise ValueError("outputs must be contiguous [B, H, N, D]")
+    rc = _lib.dit_qkv_to_head_major(qkv.data_ptr(), qkv.stride(0), qkv.stride(1), B, N, H, D,
+                                    outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(),
+                                    _stream_ptr(stream))
+    _check(rc, "dit_qkv_to_head_major")
+    return outs
+
+
+def check_watchdog(stream=None):
+    """Synchronise and read/clear the device status word: (status, info[4])."""
+    info = (ctypes.c_uint32 * 4)()
+    rc = _lib.dit_check_watchdog(_stream_ptr(stream), info)
+    return rc, list(info)

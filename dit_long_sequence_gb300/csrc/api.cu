@@ -1,0 +1,257 @@
+// api.cu -- the extern "C" entry points of libditattn.so (include/dit_attn.h).
+//
+// Host side only: argument / stride / alignment validation before anything is
+// enqueued, TMA descriptor encoding for the strided Q/K/V views, the device
+// status word read by dit_check_watchdog(), and the kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "dit_attn.h"
+#include "internal.h"
+
+namespace dit {
+
+// Device status word: [0] code, [1] block, [2] warp role, [3] wait site.
+__device__ unsigned int g_status_word[4];
+
+namespace {
+
+constexpr unsigned long long kWatchdogNs = 2000000000ull;  // 2 s per bounded wait
+constexpr int kMaxDevices = 64;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+struct DeviceCache {
+    std::atomic<unsigned int*> status{nullptr};
+    std::atomic<int> sm_count{0};
+};
+DeviceCache g_dev[kMaxDevices];
+
+unsigned int* status_word(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    unsigned int* p = g_dev[dev].status.load(std::memory_order_acquire);
+    if (p == nullptr) {
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return nullptr;
+        p = static_cast<unsigned int*>(addr);
+        g_dev[dev].status.store(p, std::memory_order_release);
+    }
+    return p;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A [B, N, H, D] bf16 view as a 4-D TMA map (D, N, H, B), box (64, 128, 1, 1),
+// 128-byte swizzle.  Rows n >= n_rows are outside the map and read as zeros.
+dit_status_t encode_view(CUtensorMap* map, const void* base, const dit_strides4_t& s, int B, int n_rows, int H,
+                         int D) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return DIT_ERR_CUDA;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(n_rows > 0 ? n_rows : 1),
+                                static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.n) * 2, static_cast<cuuint64_t>(s.h) * 2,
+                                   static_cast<cuuint64_t>(s.b) * 2};
+    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DIT_OK : DIT_ERR_INVALID_ARG;
+}
+
+// b, n, h strides of a bf16 TMA operand: positive, 16-byte multiples, < 2^39 elements.
+dit_status_t check_tma_strides(const dit_strides4_t& s) {
+    if (s.d != 1) return DIT_ERR_UNSUPPORTED;
+    const int64_t st[3] = {s.b, s.n, s.h};
+    for (int64_t x : st) {
+        if (x <= 0 || x >= (int64_t(1) << 39)) return DIT_ERR_INVALID_ARG;
+        if (x % 8 != 0) return DIT_ERR_ALIGNMENT;
+    }
+    return DIT_OK;
+}
+
+}  // namespace
+
+int device_sm_count(int dev) {
+    if (dev >= 0 && dev < kMaxDevices) {
+        int c = g_dev[dev].sm_count.load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 148;
+    if (dev >= 0 && dev < kMaxDevices) g_dev[dev].sm_count.store(c, std::memory_order_relaxed);
+    return c;
+}
+
+}  // namespace dit
+
+using namespace dit;
+
+extern "C" {
+
+dit_status_t dit_attn_fwd(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides, int B,
+                          int Nq, int Nkv, int H, int D, int key_valid_len, float scale, void* out,
+                          dit_dtype_t out_dtype, float* lse, dit_stream_t stream) {
+    if (strides == nullptr) return DIT_ERR_INVALID_ARG;
+    if (B < 0 || Nq < 0 || Nkv < 0 || H < 0) return DIT_ERR_INVALID_ARG;
+    if (key_valid_len < 0 || key_valid_len > Nkv) return DIT_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return DIT_ERR_INVALID_ARG;
+    if (out_dtype != DIT_BF16 && out_dtype != DIT_F32) return DIT_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return DIT_ERR_UNSUPPORTED;
+    if (B > 65535 || H > 65535) return DIT_ERR_UNSUPPORTED;
+    if (B == 0 || Nq == 0 || H == 0) return DIT_OK;
+    if (out == nullptr || lse == nullptr) return DIT_ERR_INVALID_ARG;
+    const bool any_keys = key_valid_len > 0;
+    if (any_keys && (q == nullptr || k == nullptr || v == nullptr)) return DIT_ERR_INVALID_ARG;
+
+    // Output: d contiguous; b, n, h strides non-negative 16-byte multiples.
+    const dit_strides4_t& so = strides->o;
+    if (so.d != 1) return DIT_ERR_UNSUPPORTED;
+    const int64_t o_align = out_dtype == DIT_F32 ? 4 : 8;
+    if (so.b < 0 || so.n < 0 || so.h < 0) return DIT_ERR_INVALID_ARG;
+    if (so.b % o_align || so.n % o_align || so.h % o_align) return DIT_ERR_ALIGNMENT;
+    if (!aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return DIT_ERR_ALIGNMENT;
+
+    CUtensorMap tq, tk, tv;
+    std::memset(&tq, 0, sizeof tq);
+    std::memset(&tk, 0, sizeof tk);
+    std::memset(&tv, 0, sizeof tv);
+    if (any_keys) {
+        dit_status_t st;
+        if ((st = check_tma_strides(strides->q)) != DIT_OK) return st;
+        if ((st = check_tma_strides(strides->k)) != DIT_OK) return st;
+        if ((st = check_tma_strides(strides->v)) != DIT_OK) return st;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return DIT_ERR_ALIGNMENT;
+        if ((st = encode_view(&tq, q, strides->q, B, Nq, H, D)) != DIT_OK) return st;
+        if ((st = encode_view(&tk, k, strides->k, B, key_valid_len, H, D)) != DIT_OK) return st;
+        if ((st = encode_view(&tv, v, strides->v, B, key_valid_len, H, D)) != DIT_OK) return st;
+    }
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DIT_ERR_CUDA;
+    AttnArgs a;
+    a.Nq = Nq;
+    a.H = H;
+    a.kv_len = key_valid_len;
+    a.n_kv_tiles = (key_valid_len + 127) / 128;
+    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    a.out = out;
+    a.o_sb = so.b;
+    a.o_sn = so.n;
+    a.o_sh = so.h;
+    a.lse = lse;
+    a.status = status_word(dev);
+    a.timeout_ns = kWatchdogNs;
+    if (a.status == nullptr) return DIT_ERR_CUDA;
+    cudaError_t e = launch_attn_fwd(tq, tk, tv, a, B, D, out_dtype == DIT_BF16, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DIT_OK : DIT_ERR_CUDA;
+}
+
+dit_status_t dit_attn_lse_merge(const float* o_parts, int64_t o_chunk_stride, const float* lse_parts,
+                                int64_t lse_chunk_stride, int n_chunks, int B, int Nq, int H, int D, void* out,
+                                dit_dtype_t out_dtype, float* lse_out, dit_stream_t stream) {
+    if (n_chunks < 1 || n_chunks > 64) return DIT_ERR_INVALID_ARG;
+    if (B < 0 || Nq < 0 || H < 0) return DIT_ERR_INVALID_ARG;
+    if (out_dtype != DIT_BF16 && out_dtype != DIT_F32) return DIT_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return DIT_ERR_UNSUPPORTED;
+    if (B == 0 || Nq == 0 || H == 0) return DIT_OK;
+    if (o_parts == nullptr || lse_parts == nullptr || out == nullptr) return DIT_ERR_INVALID_ARG;
+    const int64_t rows = static_cast<int64_t>(B) * Nq * H;
+    if (n_chunks > 1) {
+        if (o_chunk_stride < rows * D || lse_chunk_stride < rows) return DIT_ERR_INVALID_ARG;
+    }
+    if (o_chunk_stride < 0 || lse_chunk_stride < 0) return DIT_ERR_INVALID_ARG;
+    if (o_chunk_stride % 4 != 0) return DIT_ERR_ALIGNMENT;
+    if (!aligned16(o_parts) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse_parts) & 3u) ||
+        (reinterpret_cast<uintptr_t>(lse_out) & 3u))
+        return DIT_ERR_ALIGNMENT;
+    MergeArgs a;
+    a.o_parts = o_parts;
+    a.o_chunk_stride = o_chunk_stride;
+    a.lse_parts = lse_parts;
+    a.lse_chunk_stride = lse_chunk_stride;
+    a.n_chunks = n_chunks;
+    a.B = B;
+    a.Nq = Nq;
+    a.H = H;
+    a.out = out;
+    a.lse_out = lse_out;
+    cudaError_t e = launch_lse_merge(a, D, out_dtype == DIT_BF16, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DIT_OK : DIT_ERR_CUDA;
+}
+
+dit_status_t dit_qkv_to_head_major(const void* qkv, int64_t stride_b, int64_t stride_n, int B, int N, int H, int D,
+                                   void* q_out, void* k_out, void* v_out, dit_stream_t stream) {
+    if (B < 0 || N < 0 || H < 0 || D < 0) return DIT_ERR_INVALID_ARG;
+    if (D % 8 != 0) return DIT_ERR_UNSUPPORTED;
+    if (B == 0 || N == 0 || H == 0 || D == 0) return DIT_OK;
+    if (qkv == nullptr || q_out == nullptr || k_out == nullptr || v_out == nullptr) return DIT_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(3) * H * D > (int64_t(1) << 28)) return DIT_ERR_UNSUPPORTED;
+    if (stride_b < 0 || stride_n < 0) return DIT_ERR_INVALID_ARG;
+    if (stride_b % 8 || stride_n % 8) return DIT_ERR_ALIGNMENT;
+    if (!aligned16(qkv) || !aligned16(q_out) || !aligned16(k_out) || !aligned16(v_out)) return DIT_ERR_ALIGNMENT;
+    LayoutArgs a;
+    a.qkv = static_cast<const uint16_t*>(qkv);
+    a.stride_b = stride_b;
+    a.stride_n = stride_n;
+    a.B = B;
+    a.N = N;
+    a.H = H;
+    a.D = D;
+    a.out[0] = static_cast<uint16_t*>(q_out);
+    a.out[1] = static_cast<uint16_t*>(k_out);
+    a.out[2] = static_cast<uint16_t*>(v_out);
+    cudaError_t e = launch_qkv_to_head_major(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DIT_OK : DIT_ERR_CUDA;
+}
+
+const char* dit_status_string(dit_status_t s) {
+    switch (s) {
+        case DIT_OK: return "DIT_OK";
+        case DIT_ERR_INVALID_ARG: return "DIT_ERR_INVALID_ARG: invalid argument";
+        case DIT_ERR_UNSUPPORTED: return "DIT_ERR_UNSUPPORTED: request outside the built configurations";
+        case DIT_ERR_ALIGNMENT: return "DIT_ERR_ALIGNMENT: pointer or stride breaks the 16-byte rules";
+        case DIT_ERR_CUDA: return "DIT_ERR_CUDA: a CUDA call failed";
+        case DIT_ERR_TIMEOUT: return "DIT_ERR_TIMEOUT: a bounded in-kernel wait ran out";
+    }
+    return "unknown dit_status_t";
+}
+
+dit_status_t dit_check_watchdog(dit_stream_t stream, uint32_t info[4]) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DIT_ERR_CUDA;
+    unsigned int host[4] = {0, 0, 0, 0};
+    if (cudaMemcpyFromSymbol(host, g_status_word, sizeof host) != cudaSuccess) return DIT_ERR_CUDA;
+    if (host[0] != 0) {
+        const unsigned int zero[4] = {0, 0, 0, 0};
+        if (cudaMemcpyToSymbol(g_status_word, zero, sizeof zero) != cudaSuccess) return DIT_ERR_CUDA;
+    }
+    if (info != nullptr)
+        for (int i = 0; i < 4; ++i) info[i] = host[i];
+    return host[0] == 0 ? DIT_OK : DIT_ERR_TIMEOUT;
+}
+
+uint32_t dit_version(void) { return (0u << 16) | 1u; }
+
+}  // extern "C"

@@ -1,0 +1,414 @@
+// attn_fwd.cu -- dense bidirectional attention forward with per-row LSE,
+// sm_103a, TMA + tcgen05 (TMEM accumulators), warp-specialised.
+//
+// Computes, for every (b, h) head and query row i,
+//     O[b,i,h,:] = sum_j softmax_j(scale * q_i . k_j) v_j,
+//     LSE[b,h,i] = ln sum_j exp(scale * q_i . k_j),
+// over the valid keys j < kv_len -- the inner attention of "Scaling Video
+// Generation Across NVL72 rack with TensorRT-LLM" ("The Scaling Challenge in
+// Video Generation": dense, unmasked, bidirectional; "Attention2D
+// Parallelism" / "Local Attention": output plus LSE so partial passes merge).
+// The key-only tail mask follows "8 卡怎么分 token：LTX-2 序列并行的 all2all
+// 到底搬了什么" ("构造 padding mask").
+//
+// CTA = 256 query rows of one (b, h) as two 128-row tiles, 12 warps:
+//   warps 0-3  softmax for query tile 0 (one TMEM lane = one row per thread)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    tcgen05.mma issuer (one thread); owns the TMEM allocation
+//   warp  9    TMA producer (one thread): Q once, then K_0, V_0, K_1, V_1, ...
+//              through a ring of STAGES shared-memory slots
+//   warps 10-11 idle (they complete the third warpgroup)
+// Registers: launched at 168 per thread (3 warps per SM sub-partition); the
+// softmax warpgroups raise theirs to 208 and the third warpgroup drops to 88,
+// which sums to the launch budget exactly (256*208 + 128*88 = 384*168).
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
+// P_t (bf16, 64 columns) is written by the softmax warps over the first half of
+// S_t and fed to the PV product as the TMEM A operand.
+//
+// Per KV tile j the MMA thread issues, in order,
+//   PV0(j-1 ... ) and QK0(j+1) once P0(j) is ready, then PV1(j), QK1(j+1) once
+//   P1(j) is ready -- so the tensor pipe runs one tile's products while the
+//   other tile's softmax runs.  Products issued by one thread execute in order,
+//   which makes writing S_t(j+1) over P_t(j) safe after PV_t(j).
+//
+// Online softmax in log2 units with a lazy rescale: the running max m of a row
+// only moves (and O, l are rescaled by 2^(m_old - m_new)) when the tile max
+// exceeds m by more than 8; otherwise exponents use the stale m, so every P
+// stays <= 2^8 and the final O / l is exact because both use the same m.
+//
+// Keys j >= kv_len are outside the K/V tensor maps (zero fill) and masked to
+// -inf in the last tile, so pad rows are never read.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dit {
+namespace {
+
+constexpr int kBM = 128;           // query rows per tile
+constexpr int kBN = 128;           // keys per KV tile
+constexpr int kThreads = 384;
+constexpr uint32_t kSoftmaxRegs = 208;
+constexpr uint32_t kOtherRegs = 88;
+static_assert(256 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * 168, "register split");
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct Cfg {
+    static constexpr int kTileBytes = kBM * D * 2;          // one 128 x D bf16 tile
+    static constexpr int kStages = (D == 128) ? 4 : 8;      // K/V ring slots
+    static constexpr int kBlockBytes = kBM * 128;           // 128 rows x 64 bf16 (one swizzle column)
+    // barriers
+    static constexpr int kQFull = 0;
+    static constexpr int kKVFull = 2;
+    static constexpr int kKVEmpty = kKVFull + kStages;
+    static constexpr int kSFull = kKVEmpty + kStages;
+    static constexpr int kPFull = kSFull + 2;
+    static constexpr int kOFinal = kPFull + 2;
+    static constexpr int kDrain = kOFinal + 2;
+    static constexpr int kLoadDrain = kDrain + 1;
+    static constexpr int kNumBars = kLoadDrain + 1;
+    static constexpr int kBarOffset = (2 + kStages) * kTileBytes;
+    static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kBarOffset + kNumBars * 8 + 16;
+    static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+template <int D, bool OUT_BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
+    using C = Cfg<D>;
+    constexpr int S = C::kStages;
+    constexpr int TILE = C::kTileBytes;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t sQ = s_base;                 // Q tile t at sQ + t*TILE
+    const uint32_t sRing = s_base + 2 * TILE;   // slot s at sRing + s*TILE
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* never_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);  // stays 0
+    auto bar = [&](int i) -> uint32_t { return smem_u32(bars + i); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int h = blockIdx.y;
+    const int b = blockIdx.z;
+    const int q_row0 = blockIdx.x * (2 * kBM);
+    const int n_tiles = a.n_kv_tiles;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::kQFull + 0), 1);
+        mbar_init(bar(C::kQFull + 1), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar(C::kKVFull + s), 1);
+            mbar_init(bar(C::kKVEmpty + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(C::kSFull + t), 1);
+            mbar_init(bar(C::kPFull + t), 128);
+            mbar_init(bar(C::kOFinal + t), 1);
+        }
+        mbar_init(bar(C::kDrain), 1);
+        mbar_init(bar(C::kLoadDrain), 1);
+        *abort_flag = 0;
+        *never_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 8) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Watchdog wd{a.status, a.timeout_ns, abort_flag};
+    // A second watchdog view that ignores the abort flag: used only to wait
+    // (bounded) for work already in flight while winding down.
+    const Watchdog wd_drain{a.status, a.timeout_ns, never_flag};
+
+    if (warp >= 10) {
+        regs_decrease<kOtherRegs>();  // idle warps
+    } else if (warp == 9) {
+        regs_decrease<kOtherRegs>();
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && n_tiles > 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            for (int t = 0; t < 2; ++t) {
+                mbar_arrive_expect_tx(bar(C::kQFull + t), TILE);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d(sQ + t * TILE + c * C::kBlockBytes, &tm_q, bar(C::kQFull + t), c * 64,
+                                q_row0 + t * kBM, h, b);
+            }
+            const int total = 2 * n_tiles;
+            int issued = 0;
+            for (int i = 0; i < total; ++i) {
+                const int slot = i % S;
+                const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
+                if (!wait_bounded(bar(C::kKVEmpty + slot), ph ^ 1u, wd, ROLE_LOAD, SITE_KV_EMPTY)) break;
+                mbar_arrive_expect_tx(bar(C::kKVFull + slot), TILE);
+                const CUtensorMap* tm = (i & 1) ? &tm_v : &tm_k;
+                const uint32_t dst = sRing + slot * TILE;
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d(dst + c * C::kBlockBytes, tm, bar(C::kKVFull + slot), c * 64, (i >> 1) * kBN, h, b);
+                issued = i + 1;
+            }
+            if (issued < total || *abort_flag) {
+                // Winding down: wait (bounded) until every copy issued has landed.
+                for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
+                    wait_bounded(bar(C::kKVFull + i % S), static_cast<uint32_t>(i / S) & 1u, wd_drain,
+                                 ROLE_LOAD, SITE_LOAD_DRAIN);
+                wait_bounded(bar(C::kQFull + 0), 0, wd_drain, ROLE_LOAD, SITE_LOAD_DRAIN);
+                wait_bounded(bar(C::kQFull + 1), 0, wd_drain, ROLE_LOAD, SITE_LOAD_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 8) {
+        regs_decrease<kOtherRegs>();
+        // ------------------------------------------------------------- MMA issuer
+        if (lane == 0 && n_tiles > 0) {
+            constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false);
+            constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, true);
+            const uint32_t tS0 = tmem, tS1 = tmem + 128;
+            const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + D;
+
+            // S_t = Q_t K^T : A = Q (K-major), B = K (K-major), K-dim = D.
+            auto issue_qk = [&](uint32_t tS, uint32_t q_addr, uint32_t k_addr) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+                    umma_ss(tS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+                            kIdescQK, kk > 0 ? 1u : 0u);
+                }
+            };
+            // O_t (+)= P_t V : A = P (TMEM, bf16 pairs), B = V (MN-major), K-dim = 128 keys.
+            auto issue_pv = [&](uint32_t tO, uint32_t tP, uint32_t v_addr, bool accumulate) {
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    umma_ts(tO, tP + kk * 8, sdesc_sw128(v_addr + kk * 16 * 128, C::kBlockBytes, 1024), kIdescPV,
+                            (accumulate || kk > 0) ? 1u : 0u);
+            };
+
+            bool ok = wait_bounded(bar(C::kQFull + 0), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
+                      wait_bounded(bar(C::kQFull + 1), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
+                      wait_bounded(bar(C::kKVFull + 0), 0, wd, ROLE_MMA, SITE_KV_FULL);
+            if (ok) {
+                tc_fence_after();
+                issue_qk(tS0, sQ, sRing);
+                umma_commit(bar(C::kSFull + 0));
+                issue_qk(tS1, sQ + TILE, sRing);
+                umma_commit(bar(C::kSFull + 1));
+                umma_commit(bar(C::kKVEmpty + 0));
+            }
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int iv = 2 * j + 1, ik = 2 * j + 2;
+                const uint32_t v_addr = sRing + (iv % S) * TILE;
+                const uint32_t k_addr = sRing + (ik % S) * TILE;
+                const bool more = j + 1 < n_tiles;
+                const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+                ok = wait_bounded(bar(C::kKVFull + iv % S), static_cast<uint32_t>(iv / S) & 1u, wd, ROLE_MMA,
+                                  SITE_KV_FULL) &&
+                     wait_bounded(bar(C::kPFull + 0), ph, wd, ROLE_MMA, SITE_P_FULL);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(tO0, tS0, v_addr, j > 0);
+                if (more) {
+                    ok = wait_bounded(bar(C::kKVFull + ik % S), static_cast<uint32_t>(ik / S) & 1u, wd, ROLE_MMA,
+                                      SITE_KV_FULL);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_qk(tS0, sQ, k_addr);
+                    umma_commit(bar(C::kSFull + 0));
+                } else {
+                    umma_commit(bar(C::kOFinal + 0));
+                }
+                ok = wait_bounded(bar(C::kPFull + 1), ph, wd, ROLE_MMA, SITE_P_FULL);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(tO1, tS1, v_addr, j > 0);
+                umma_commit(bar(C::kKVEmpty + iv % S));
+                if (more) {
+                    issue_qk(tS1, sQ + TILE, k_addr);
+                    umma_commit(bar(C::kSFull + 1));
+                    umma_commit(bar(C::kKVEmpty + ik % S));
+                } else {
+                    umma_commit(bar(C::kOFinal + 1));
+                }
+            }
+            // Every product issued must finish before TMEM is released.
+            umma_commit(bar(C::kDrain));
+            wait_bounded(bar(C::kDrain), 0, wd_drain, ROLE_MMA, SITE_DRAIN);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------- softmax warps
+        regs_increase<kSoftmaxRegs>();
+        const int t = warp >> 2;    // query tile
+        const int wq = warp & 3;    // TMEM lane quadrant
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + t * 128;
+        const uint32_t tO = tmem + lane_off + 256 + t * D;
+        const int row = q_row0 + t * kBM + wq * 32 + lane;
+        const float sl2 = a.scale_log2;
+        float m = -INFINITY;  // running max of scale*log2(e)*s (possibly stale)
+        float l = 0.f;        // running sum of 2^(s*sl2 - m)
+        bool ok = true;
+
+        for (int j = 0; j < n_tiles; ++j) {
+            ok = wait_bounded(bar(C::kSFull + t), static_cast<uint32_t>(j) & 1u, wd, ROLE_SOFTMAX, SITE_S_FULL);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
+            tmem_ld_wait();
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+
+            const int valid = a.kv_len - j * kBN;
+            if (valid < kBN) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c >= valid) s[c] = -INFINITY;
+            }
+            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+            for (int c = 4; c < 128; c += 4) {
+                mx0 = fmaxf(mx0, s[c]);
+                mx1 = fmaxf(mx1, s[c + 1]);
+                mx2 = fmaxf(mx2, s[c + 2]);
+                mx3 = fmaxf(mx3, s[c + 3]);
+            }
+            const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+            if (j == 0) {
+                m = m_tile;
+            } else {
+                const bool need = m_tile > m + kRescaleThreshold;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float m_new = need ? m_tile : m;
+                    const float alpha = ex2_approx(m - m_new);
+                    l *= alpha;
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + cc * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tO + cc * 32, o);
+                    }
+                    m = m_new;
+                }
+            }
+            const float neg_m = -m;
+            float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2_approx(fmaf(s[32 * cc + 2 * i], sl2, neg_m));
+                    const float p1 = ex2_approx(fmaf(s[32 * cc + 2 * i + 1], sl2, neg_m));
+                    ls0 += p0;
+                    ls1 += p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(tS + cc * 16, pk);
+            }
+            l += ls0 + ls1;
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(C::kPFull + t));
+        }
+
+        // ---------------------------------------------------------------- epilogue
+        if (ok && n_tiles > 0) {
+            ok = wait_bounded(bar(C::kOFinal + t), 0, wd, ROLE_SOFTMAX, SITE_O_FINAL);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) tc_fence_after();
+        }
+        if (ok) {
+            const bool in_range = row < a.Nq;
+            const int64_t o_off = static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(row) * a.o_sn +
+                                  static_cast<int64_t>(h) * a.o_sh;
+            const float inv_l = n_tiles > 0 ? 1.f / l : 0.f;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t o[32];
+                if (n_tiles > 0) {
+                    tmem_ld32(tO + cc * 32, o);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                if (in_range) {
+                    if constexpr (OUT_BF16) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + o_off + cc * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv_l, __uint_as_float(o[8 * v4 + 1]) * inv_l);
+                            w.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv_l, __uint_as_float(o[8 * v4 + 3]) * inv_l);
+                            w.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv_l, __uint_as_float(o[8 * v4 + 5]) * inv_l);
+                            w.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv_l, __uint_as_float(o[8 * v4 + 7]) * inv_l);
+                            dst[v4] = w;
+                        }
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + o_off + cc * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4)
+                            dst[v4] = make_float4(__uint_as_float(o[4 * v4 + 0]) * inv_l, __uint_as_float(o[4 * v4 + 1]) * inv_l,
+                                                  __uint_as_float(o[4 * v4 + 2]) * inv_l, __uint_as_float(o[4 * v4 + 3]) * inv_l);
+                    }
+                }
+            }
+            if (in_range) {
+                const float lse = n_tiles > 0 ? (m + log2f(l)) * kLn2 : -INFINITY;
+                a.lse[(static_cast<int64_t>(b) * a.H + h) * a.Nq + row] = lse;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& args,
+                        int B, cudaStream_t stream) {
+    auto kern = attn_fwd_kernel<D, BF16>;
+    const int smem = Cfg<D>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((args.Nq + 2 * kBM - 1) / (2 * kBM), args.H, B);
+    kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const AttnArgs& args, int B, int D, bool out_bf16, cudaStream_t stream) {
+    if (D == 128) return out_bf16 ? launch_impl<128, true>(tq, tk, tv, args, B, stream)
+                                  : launch_impl<128, false>(tq, tk, tv, args, B, stream);
+    return out_bf16 ? launch_impl<64, true>(tq, tk, tv, args, B, stream)
+                    : launch_impl<64, false>(tq, tk, tv, args, B, stream);
+}
+
+}  // namespace dit

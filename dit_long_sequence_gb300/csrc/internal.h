@@ -1,0 +1,59 @@
+// internal.h -- launch-side declarations shared by the kernel translation
+// units and the C-ABI layer (api.cu).  Not part of the public interface.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dit {
+
+// Warp roles and wait sites reported by the watchdog (status words 2 and 3).
+enum WatchRole : uint32_t { ROLE_SOFTMAX = 1, ROLE_MMA = 2, ROLE_LOAD = 3 };
+enum WatchSite : uint32_t {
+    SITE_Q_FULL = 1, SITE_KV_FULL = 2, SITE_KV_EMPTY = 3, SITE_S_FULL = 4, SITE_P_FULL = 5,
+    SITE_O_FINAL = 6, SITE_DRAIN = 7, SITE_LOAD_DRAIN = 8
+};
+
+struct AttnArgs {
+    int Nq;            // query rows
+    int H;             // heads
+    int kv_len;        // valid keys (keys >= kv_len are masked)
+    int n_kv_tiles;    // ceil(kv_len / 128)
+    float scale_log2;  // scale * log2(e)
+    void* out;         // O, fp32 or bf16
+    int64_t o_sb, o_sn, o_sh;  // O element strides
+    float* lse;        // [B, H, Nq]
+    unsigned int* status;      // device status word (4 x u32)
+    unsigned long long timeout_ns;
+};
+
+// Attention forward.  grid = (ceil(Nq/256), H, B), 320 threads.
+cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const AttnArgs& args, int B, int D, bool out_bf16, cudaStream_t stream);
+
+struct MergeArgs {
+    const float* o_parts;
+    int64_t o_chunk_stride;
+    const float* lse_parts;
+    int64_t lse_chunk_stride;
+    int n_chunks;
+    int B, Nq, H;
+    void* out;
+    float* lse_out;
+};
+
+cudaError_t launch_lse_merge(const MergeArgs& args, int D, bool out_bf16, cudaStream_t stream);
+
+struct LayoutArgs {
+    const uint16_t* qkv;
+    int64_t stride_b, stride_n;
+    int B, N, H, D;
+    uint16_t* out[3];
+};
+
+cudaError_t launch_qkv_to_head_major(const LayoutArgs& args, cudaStream_t stream);
+
+int device_sm_count(int device);
+
+}  // namespace dit

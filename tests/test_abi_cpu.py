@@ -1,0 +1,119 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library loads and exports every entry point include/dit_attn.h declares,
+and every argument check returns its status before anything touches a device
+(the pointers passed here are never dereferenced).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dit_long_sequence_gb300 import build
+    build.build()
+    from dit_long_sequence_gb300 import binding
+    return binding
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dit_attn.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(dit_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"dit_attn_fwd", "dit_attn_lse_merge", "dit_qkv_to_head_major"} <= set(names)
+    for n in names:
+        assert hasattr(lib.raw(), n), n
+    assert set(lib.EXPORTS) <= set(names)
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.raw().dit_status_string(s).startswith(b"DIT_")
+    assert lib.raw().dit_version() >= 1
+
+
+FAKE = 0x1000_0000  # 16-byte aligned, never dereferenced
+
+
+def _fwd(lib, **kw):
+    st = lib.AttnStrides(lib.Strides4(8 * 128 * 4, 4 * 128, 128, 1), lib.Strides4(8 * 128 * 4, 4 * 128, 128, 1),
+                         lib.Strides4(8 * 128 * 4, 4 * 128, 128, 1), lib.Strides4(8 * 128 * 4, 4 * 128, 128, 1))
+    args = dict(q=FAKE, k=FAKE, v=FAKE, st=st, B=1, Nq=8, Nkv=8, H=4, D=128, kvl=8, scale=0.088, out=FAKE,
+                dt=lib.DIT_F32, lse=FAKE)
+    args.update(kw)
+    s = args["st"]
+    return lib.raw().dit_attn_fwd(args["q"], args["k"], args["v"], ctypes.byref(s), args["B"], args["Nq"],
+                                  args["Nkv"], args["H"], args["D"], args["kvl"], args["scale"], args["out"],
+                                  args["dt"], args["lse"], None)
+
+
+def test_attn_fwd_argument_checks(lib):
+    E = lib
+    assert _fwd(lib, D=96) == E.DIT_ERR_UNSUPPORTED
+    assert _fwd(lib, D=256) == E.DIT_ERR_UNSUPPORTED
+    assert _fwd(lib, kvl=9) == E.DIT_ERR_INVALID_ARG
+    assert _fwd(lib, kvl=-1) == E.DIT_ERR_INVALID_ARG
+    assert _fwd(lib, scale=0.0) == E.DIT_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("nan")) == E.DIT_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("inf")) == E.DIT_ERR_INVALID_ARG
+    assert _fwd(lib, B=-1) == E.DIT_ERR_INVALID_ARG
+    assert _fwd(lib, out=None) == E.DIT_ERR_INVALID_ARG
+    assert _fwd(lib, lse=None) == E.DIT_ERR_INVALID_ARG
+    assert _fwd(lib, q=None) == E.DIT_ERR_INVALID_ARG
+    assert _fwd(lib, dt=7) == E.DIT_ERR_INVALID_ARG
+    assert _fwd(lib, q=FAKE + 8) == E.DIT_ERR_ALIGNMENT
+    assert _fwd(lib, out=FAKE + 4) == E.DIT_ERR_ALIGNMENT
+    bad = lib.Strides4(8 * 128 * 4, 4 * 128 + 4, 128, 1)   # n stride not 16-byte aligned
+    good = lib.Strides4(8 * 128 * 4, 4 * 128, 128, 1)
+    assert _fwd(lib, st=lib.AttnStrides(bad, good, good, good)) == E.DIT_ERR_ALIGNMENT
+    nd = lib.Strides4(8 * 128 * 4, 4 * 128, 128, 2)      # d not contiguous
+    assert _fwd(lib, st=lib.AttnStrides(good, good, nd, good)) == E.DIT_ERR_UNSUPPORTED
+    # zero-size problems are a no-op that succeeds without touching memory
+    assert _fwd(lib, B=0, q=None, out=None, lse=None) == E.DIT_OK
+    assert _fwd(lib, Nq=0) == E.DIT_OK
+
+
+def test_merge_argument_checks(lib):
+    f = lib.raw().dit_attn_lse_merge
+    ok_args = (FAKE, 1 * 8 * 4 * 128, FAKE, 1 * 4 * 8, 2, 1, 8, 4, 128, FAKE, lib.DIT_F32, FAKE, None)
+
+    def call(**kw):
+        a = list(ok_args)
+        names = ["o", "ocs", "l", "lcs", "n", "B", "Nq", "H", "D", "out", "dt", "lo", "s"]
+        for k_, v_ in kw.items():
+            a[names.index(k_)] = v_
+        return f(*a)
+    assert call(n=0) == lib.DIT_ERR_INVALID_ARG
+    assert call(n=65) == lib.DIT_ERR_INVALID_ARG
+    assert call(D=32) == lib.DIT_ERR_UNSUPPORTED
+    assert call(ocs=8) == lib.DIT_ERR_INVALID_ARG      # chunks would overlap
+    assert call(o=None) == lib.DIT_ERR_INVALID_ARG
+    assert call(o=FAKE + 4) == lib.DIT_ERR_ALIGNMENT
+    assert call(B=0) == lib.DIT_OK
+
+
+def test_layout_argument_checks(lib):
+    f = lib.raw().dit_qkv_to_head_major
+    assert f(FAKE, 0, 3 * 4 * 12, 1, 8, 4, 12, FAKE, FAKE, FAKE, None) == lib.DIT_ERR_UNSUPPORTED  # D % 8
+    assert f(FAKE, 0, 3 * 4 * 64 + 4, 1, 8, 4, 64, FAKE, FAKE, FAKE, None) == lib.DIT_ERR_ALIGNMENT
+    assert f(None, 0, 3 * 4 * 64, 1, 8, 4, 64, FAKE, FAKE, FAKE, None) == lib.DIT_ERR_INVALID_ARG
+    assert f(FAKE, 0, 3 * 4 * 64, 1, 8, 4, 64, FAKE + 2, FAKE, FAKE, None) == lib.DIT_ERR_ALIGNMENT
+    assert f(FAKE, 0, 3 * 4 * 64, 1, 0, 4, 64, FAKE, FAKE, FAKE, None) == lib.DIT_OK
+
+
+def test_product_path_never_imports_oracle():
+    pkg = os.path.join(ROOT, "dit_long_sequence_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, fn
+                assert "attn_oracle" not in text, fn

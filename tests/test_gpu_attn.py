@@ -1,0 +1,148 @@
+"""GPU parity of dit_attn_fwd (through the C ABI) against the fp64 oracle.
+
+Small cases are compared element by element on every row; they span several
+256-row query blocks and 128-key tiles with ragged tails in both.  The
+model-shaped workloads are compared on >= 1024 sampled query rows per head
+against all keys, in the launch configuration the benchmark times.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from dit_long_sequence_gb300 import workloads as wl
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev():
+    return torch.device("cuda:0")
+
+
+def _attn(q, k, v, **kw):
+    import dit_long_sequence_gb300 as dl
+    return dl.attn_fwd(q, k, v, **kw)
+
+
+@pytest.mark.parametrize("B,Nq,Nkv,H,D,kvl,seed", [
+    (1, 1024, 1024, 2, 64, None, 0),      # the tiny workload, whole
+    (1, 256, 256, 1, 128, None, 1),       # exactly one block, two key tiles
+    (1, 300, 300, 2, 128, None, 2),       # ragged query block and key tile
+    (2, 257, 383, 3, 64, None, 3),        # cross lengths, D = 64
+    (1, 520, 700, 2, 128, 555, 4),        # key mask inside a tile
+    (1, 129, 260, 1, 128, 256, 5),        # mask exactly on a tile edge
+    (1, 64, 300, 2, 128, 1, 6),           # one valid key
+    (1, 1, 1, 1, 128, None, 7),           # single query, single key
+    (3, 700, 129, 2, 64, None, 8),        # one key past a tile
+])
+def test_attn_matches_oracle_small(B, Nq, Nkv, H, D, kvl, seed):
+    q, k, v, _ = wl.make_qkv(B, Nq, H, D, seed, device=_dev(), Nkv=Nkv)
+    O, L = _attn(q, k, v, key_valid_len=kvl)
+    torch.cuda.synchronize()
+    Or, Lr = parity.oracle_full(q, k, v, key_valid_len=kvl)
+    parity.compare(O.double().cpu().numpy(), L.double().cpu().numpy(), Or, Lr, head_axes=(0, 2))
+
+
+def test_fused_strided_views_and_bf16_out():
+    B, N, H, D = 2, 600, 4, 128
+    q, k, v, buf = wl.make_qkv(B, N, H, D, seed=9, device=_dev(), fused=True)
+    assert q.stride(1) == 3 * H * D
+    O, L = _attn(q, k, v)
+    Ob, Lb = _attn(q, k, v, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    Or, Lr = parity.oracle_full(q, k, v)
+    parity.compare(O.double().cpu().numpy(), L.double().cpu().numpy(), Or, Lr, head_axes=(0, 2))
+    # bf16 output only adds its own rounding (<= 2^-9 relative)
+    parity.compare(Ob.double().cpu().numpy(), Lb.double().cpu().numpy(), Or, Lr, head_axes=(0, 2))
+    assert torch.equal(L, Lb)
+
+
+def test_strided_output():
+    B, N, H, D = 1, 384, 2, 128
+    q, k, v, _ = wl.make_qkv(B, N, H, D, seed=10, device=_dev())
+    big = torch.full((B, N, H, 2 * D), float("nan"), device=_dev())
+    out = big[..., :D]                     # row stride 2*D, not contiguous
+    O, L = _attn(q, k, v, out=out)
+    torch.cuda.synchronize()
+    assert torch.isnan(big[..., D:]).all(), "wrote outside the output view"
+    Or, Lr = parity.oracle_full(q, k, v)
+    parity.compare(O.double().cpu().numpy(), L.double().cpu().numpy(), Or, Lr, head_axes=(0, 2))
+
+
+def test_peaky_attention_large_outputs():
+    # Q and K share a strong rank-1 component: attention concentrates on few keys
+    # and |O| ~ 1, so the absolute gates are tight relative to the values.
+    B, N, H, D = 1, 640, 2, 128
+    g = wl.generator(_dev(), 11)
+    base = torch.randn(B, N, H, D, generator=g, device=_dev())
+    u = torch.randn(1, 1, H, D, generator=g, device=_dev())
+    w = torch.randn(B, N, H, 1, generator=g, device=_dev())
+    q = (0.3 * base + 2.0 * u).to(torch.bfloat16)
+    k = (0.3 * torch.randn(B, N, H, D, generator=g, device=_dev()) + 2.0 * w * u).to(torch.bfloat16)
+    v = torch.randn(B, N, H, D, generator=g, device=_dev()).to(torch.bfloat16)
+    O, L = _attn(q, k, v)
+    torch.cuda.synchronize()
+    Or, Lr = parity.oracle_full(q, k, v)
+    assert np.abs(Or).max() > 0.5
+    parity.compare(O.double().cpu().numpy(), L.double().cpu().numpy(), Or, Lr, head_axes=(0, 2))
+
+
+def test_pad_keys_never_read_and_deterministic():
+    B, N, H, D, kvl = 1, 700, 2, 128, 515
+    q, k, v, _ = wl.make_qkv(B, N, H, D, seed=12, device=_dev())
+    O1, L1 = _attn(q, k, v, key_valid_len=kvl)
+    O1b, L1b = _attn(q, k, v, key_valid_len=kvl)
+    k2, v2 = k.clone(), v.clone()
+    k2[:, kvl:] = float("inf")
+    v2[:, kvl:] = float("nan")
+    O2, L2 = _attn(q, k2, v2, key_valid_len=kvl)
+    torch.cuda.synchronize()
+    assert torch.equal(O1, O1b) and torch.equal(L1, L1b), "not run-to-run deterministic"
+    assert torch.equal(O1, O2) and torch.equal(L1, L2), "pad keys changed the result"
+
+
+def test_zero_valid_keys():
+    B, N, H, D = 1, 300, 2, 128
+    q, k, v, _ = wl.make_qkv(B, N, H, D, seed=13, device=_dev())
+    O, L = _attn(q, k, v, key_valid_len=0)
+    torch.cuda.synchronize()
+    assert (O == 0).all() and torch.isneginf(L).all()
+
+
+def test_scale_is_honoured():
+    B, N, H, D = 1, 256, 2, 64
+    q, k, v, _ = wl.make_qkv(B, N, H, D, seed=14, device=_dev())
+    for scale in (0.01, 0.3):
+        O, L = _attn(q, k, v, scale=scale)
+        torch.cuda.synchronize()
+        Or, Lr = parity.oracle_full(q, k, v, scale=scale)
+        parity.compare(O.double().cpu().numpy(), L.double().cpu().numpy(), Or, Lr, head_axes=(0, 2))
+
+
+def test_watchdog_clean_after_runs():
+    import dit_long_sequence_gb300 as dl
+    rc, info = dl.check_watchdog()
+    assert rc == 0, info
+
+
+def _sampled_check(w, rows_per_head=1024):
+    q, k, v, buf = wl.make_workload_inputs(w, device=_dev())
+    O, L = _attn(q, k, v, key_valid_len=w.key_valid_len)
+    torch.cuda.synchronize()
+    must = [w.N - 80, w.N - 1]
+    if w.key_valid_len is not None:
+        must += [w.key_valid_len - 1, w.key_valid_len, w.N - 1]
+    rows = wl.sample_rows(w.B, w.H, w.N, rows_per_head, seed=w.seed, must=must)
+    Og, Lg = parity.gather_rows(O, L, rows)
+    Or, Lr = parity.oracle_rows(q, k, v, rows, key_valid_len=w.key_valid_len)
+    res = parity.compare(Og, Lg, Or, Lr, head_axes=(0, 1))
+    # statistical smoke check: LSE ~ ln(valid keys) + 1/2 for N(0,1) inputs
+    assert abs(float(Lr.mean()) - (math.log(w.kv_len) + 0.5)) < 0.2
+    return res
+
+
+@pytest.mark.parametrize("name", ["ltx2_padded", "cosmos3_nano", "wan22_a14b"])
+def test_workload_sampled_rows(name):
+    _sampled_check(wl.WORKLOADS[name])
