@@ -176,7 +176,7 @@ class Step:
         self.w, self.dev, self.dl = w, dev, dl
         self.stream = torch.cuda.current_stream(dev)
         B, N, H, D = w.B, w.N, w.H, w.D
-        self.mode = "layout+attn" if w.name in ("ltx2_padded", "tiny") else (
+        self.mode = "layout+attn" if w.name.split("_h")[0] in ("ltx2_padded", "tiny") else (
             "chunked+merge" if w.kv_chunks > 1 else "attn")
         if self.mode == "layout+attn" or w.fused:
             self.fused = wl.randn_bf16((B, N, 3, H, D), w.seed, dev)
@@ -367,12 +367,17 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="ltx2_padded")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="override the head count (small profiling cases of the same kernel)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args(argv)
     from dit_long_sequence_gb300 import workloads as wl
     w = wl.WORKLOADS[args.workload]
+    if args.heads is not None:
+        import dataclasses
+        w = dataclasses.replace(w, H=args.heads, name=f"{w.name}_h{args.heads}")
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     if args.impl == "reference":
