@@ -76,14 +76,16 @@ def profiled_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle samples (every 50 ms); only samples taken
+    inside [mark_start, mark_stop] count."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.t0 = self.t1 = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
 
     def __enter__(self):
@@ -91,14 +93,22 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.6)   # let the sampler start producing before the timed region
         except Exception:
             self.proc = None
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
+
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.1)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -109,24 +119,29 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        import datetime
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax = float(parts[2])
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, cmax = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
+            if self.t0 is not None and not (self.t0 - 0.05 <= ts <= self.t1 + 0.05):
+                continue
+            sm.append(clk)
+            smax = cmax
+            for name, val in zip(names, parts[6:10]):
                 if val.lower() == "active":
                     reasons.add(name)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["no sample inside the timed region"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window_s": (self.t1 - self.t0) if self.t0 else None}
 
 
 def dist_setup(n_gpus: int):
@@ -317,10 +332,15 @@ def cpu_baseline(w, dev_inputs=None, target_s=12.0):
         return time.perf_counter() - t0, rows.size
 
     heads = min(w.H, 8)
-    t, n = run(4, heads)
-    rate = n / max(t, 1e-6)
-    rows_per_head = int(max(4, min(w.N, target_s * rate / heads)))
+    rows_per_head = 4
     t, n = run(rows_per_head, heads)
+    while t < 0.25 * target_s and rows_per_head < w.N:
+        grow = 4 if t < 0.05 * target_s else max(1.2, 0.5 * target_s / max(t, 1e-6))
+        rows_per_head = int(min(w.N, max(rows_per_head + 1, rows_per_head * grow)))
+        t, n = run(rows_per_head, heads)
+    if t < 0.6 * target_s and rows_per_head < w.N:
+        rows_per_head = int(min(w.N, rows_per_head * target_s / max(t, 1e-6)))
+        t, n = run(rows_per_head, heads)
     tflops = n * per_row / t / 1e12
     return {"value": tflops, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
             "sample": f"{n} query rows ({rows_per_head} per head, heads 0-{heads - 1} of batch 0) "
@@ -339,6 +359,8 @@ def run_reference(args, w):
     q, k, v, _ = wl.make_workload_inputs(w, device="cpu")
     for _ in range(args.warmup):
         cpu_baseline(w, (q, k, v), target_s=1.0)
+    if args.steps is None:
+        args.steps = 5
     vals = [cpu_baseline(w, (q, k, v), target_s=max(2.0, 60.0 / max(args.steps, 1))) for _ in range(args.steps)]
     value = statistics.mean(v_["value"] for v_ in vals)
     secs = sum(v_["seconds"] for v_ in vals)
@@ -364,7 +386,8 @@ def config_of(w):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about 1.5 s of timed work)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="ltx2_padded")
     ap.add_argument("--heads", type=int, default=None,
@@ -390,9 +413,13 @@ def main(argv=None):
     import dit_long_sequence_gb300 as dl
 
     step = Step(w, dev)
+    t_warm = time.perf_counter()
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
+    if args.steps is None:
+        per = (time.perf_counter() - t_warm) / args.warmup
+        args.steps = int(max(5, min(400, math.ceil(1.5 / max(per, 1e-4)))))
     rc, info = dl.check_watchdog()
     if rc != 0:
         raise RuntimeError(f"watchdog: {rc} {info}")
@@ -403,11 +430,13 @@ def main(argv=None):
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
+        clk.mark_start()
         start.record(step.stream)
         for _ in range(args.steps):
             step.run(record=True)
         stop.record(step.stream)
         torch.cuda.synchronize()
+        clk.mark_stop()
     barrier()
     ms_total = start.elapsed_time(stop)
     ms_total = reduce_max(ms_total)
@@ -447,7 +476,7 @@ def main(argv=None):
             "gpu_launches": step.launches_per_step * args.steps, "e2e": e2e, "kernels": extra,
             "pct_of_bf16_peak": 100.0 * value / world / peak}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, (step.q, step.k, step.v))
     if rank == 0:
         print(json.dumps(line))
     return 0

@@ -35,6 +35,9 @@
 // only moves (and O, l are rescaled by 2^(m_old - m_new)) when the tile max
 // exceeds m by more than 8; otherwise exponents use the stale m, so every P
 // stays <= 2^8 and the final O / l is exact because both use the same m.
+// Because the rescale is rare, the exponents of a tile are computed with the
+// running max while the tile max is still being formed; the few warps that do
+// need a rescale recompute that tile's P.
 //
 // Keys j >= kv_len are outside the K/V tensor maps (zero fill) and masked to
 // -inf in the last tile, so pad rows are never read.
@@ -262,40 +265,98 @@ __global__ void __launch_bounds__(kThreads, 1)
         float l = 0.f;        // running sum of 2^(s*sl2 - m)
         bool ok = true;
 
+        // max over 64 scores: eight 3-input max chains, then a small tree.
+        auto max64 = [](const float* v) {
+            float t8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) t8[k] = max3f(v[k], v[8 + k], v[16 + k]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) t8[k] = max3f(t8[k], v[24 + k], v[32 + k]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) t8[k] = max3f(t8[k], v[40 + k], v[48 + k]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) t8[k] = fmaxf(t8[k], v[56 + k]);
+            return max3f(max3f(t8[0], t8[1], t8[2]), max3f(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
+        };
+        // P = 2^(s*sl2 - m_use) for 64 scores -> 32 bf16x2 TMEM columns at tP; returns sum P.
+        auto exp_store = [&](const float* v, uint32_t tP, float m_use) {
+            const float neg_m = -m_use;
+            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float x0, x1;
+                    ffma2_bc(x0, x1, v[32 * cc + 2 * i], v[32 * cc + 2 * i + 1], sl2, neg_m);
+                    const float p0 = ex2_approx(x0);
+                    const float p1 = ex2_approx(x1);
+                    if (i & 1) fadd2_acc(b0, b1, p0, p1);
+                    else fadd2_acc(a0, a1, p0, p1);
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(tP + cc * 16, pk);
+            }
+            return (a0 + a1) + (b0 + b1);
+        };
+
         for (int j = 0; j < n_tiles; ++j) {
             ok = wait_bounded(bar(C::kSFull + t), static_cast<uint32_t>(j) & 1u, wd, ROLE_SOFTMAX, SITE_S_FULL);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
 
+            // S row in two halves; the second lands while the first is processed.
             uint32_t sr[4][32];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
-            tmem_ld_wait();
+            tmem_ld32(tS + 0, sr[0]);
+            tmem_ld32(tS + 32, sr[1]);
+            tmem_ld_wait_dep(sr[0]);
+            reg_dep(sr[1]);
+            tmem_ld32(tS + 64, sr[2]);
+            tmem_ld32(tS + 96, sr[3]);
+            const int valid = a.kv_len - j * kBN;   // >= 1
             float s[128];
 #pragma unroll
-            for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
-
-            const int valid = a.kv_len - j * kBN;
-            if (valid < kBN) {
+            for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+            if (valid < 64) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
+                for (int c = 0; c < 64; ++c)
                     if (c >= valid) s[c] = -INFINITY;
             }
-            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-            for (int c = 4; c < 128; c += 4) {
-                mx0 = fmaxf(mx0, s[c]);
-                mx1 = fmaxf(mx1, s[c + 1]);
-                mx2 = fmaxf(mx2, s[c + 2]);
-                mx3 = fmaxf(mx3, s[c + 3]);
-            }
-            const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+            const float mxA = max64(s);
             if (j == 0) {
-                m = m_tile;
+                // First tile: no running max yet, so take the tile max first.
+                tmem_ld_wait_dep(sr[2]);
+                reg_dep(sr[3]);
+#pragma unroll
+                for (int c = 64; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+                if (valid < 128) {
+#pragma unroll
+                    for (int c = 64; c < 128; ++c)
+                        if (c >= valid) s[c] = -INFINITY;
+                }
+                m = fmaxf(mxA, max64(s + 64)) * sl2;
+                l = exp_store(s, tS, m) + exp_store(s + 64, tS + 32, m);
             } else {
+                // Exponents with the running max while the tile max is formed; a
+                // row whose max grew by more than the threshold redoes them below.
+                float lA = exp_store(s, tS, m);
+                tmem_ld_wait_dep(sr[2]);
+                reg_dep(sr[3]);
+#pragma unroll
+                for (int c = 64; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+                if (valid < 128) {
+#pragma unroll
+                    for (int c = 64; c < 128; ++c)
+                        if (c >= valid) s[c] = -INFINITY;
+                }
+                const float mxB = max64(s + 64);
+                float lB = exp_store(s + 64, tS + 32, m);
+                const float m_tile = fmaxf(mxA, mxB) * sl2;
                 const bool need = m_tile > m + kRescaleThreshold;
                 if (__any_sync(0xffffffffu, need)) {
+                    // O holds PV(j-1) already (S(j) was committed after it).
+                    tmem_st_wait();
                     const float m_new = need ? m_tile : m;
                     const float alpha = ex2_approx(m - m_new);
                     l *= alpha;
@@ -303,30 +364,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t o[32];
                         tmem_ld32(tO + cc * 32, o);
-                        tmem_ld_wait();
+                        tmem_ld_wait_dep(o);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
                         tmem_st32(tO + cc * 32, o);
                     }
                     m = m_new;
+                    lA = exp_store(s, tS, m);
+                    lB = exp_store(s + 64, tS + 32, m);
                 }
+                l += lA + lB;
             }
-            const float neg_m = -m;
-            float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2_approx(fmaf(s[32 * cc + 2 * i], sl2, neg_m));
-                    const float p1 = ex2_approx(fmaf(s[32 * cc + 2 * i + 1], sl2, neg_m));
-                    ls0 += p0;
-                    ls1 += p1;
-                    pk[i] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16(tS + cc * 16, pk);
-            }
-            l += ls0 + ls1;
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(C::kPFull + t));
