@@ -208,7 +208,9 @@ class Step:
         self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         if self.mode == "chunked+merge":
             n = w.kv_chunks
-            self.o_parts = torch.empty((n, B, N, H, D), dtype=torch.float32, device=dev)
+            # per-row interleaved partials [B, N, H, n, D]: the merge reads one stream
+            self.o_buf = torch.empty((B, N, H, n, D), dtype=torch.float32, device=dev)
+            self.o_parts = self.o_buf.permute(3, 0, 1, 2, 4)
             self.l_parts = torch.empty((n, B, H, N), dtype=torch.float32, device=dev)
         self.launches_per_step = {"layout+attn": 2, "attn": 1, "chunked+merge": w.kv_chunks + 1}[self.mode]
         self.attn_events = []
@@ -264,13 +266,17 @@ class Step:
         return statistics.mean(times) / per if times else float("nan")
 
 
-def time_merge_kernel(dev, B, N, H, D, n_chunks=9, reps=5):
-    """HBM roofline of dit_attn_lse_merge on ring-style partials of this shape."""
+def time_merge_kernel(dev, B, N, H, D, n_chunks=9, reps=5, interleaved=True):
+    """HBM roofline of dit_attn_lse_merge on ring-style partials of this shape
+    (chunks interleaved per row, or chunk-major)."""
     import torch
     import dit_long_sequence_gb300 as dl
     from dit_long_sequence_gb300 import workloads as wl
     g = wl.generator(dev, 77)
-    o = torch.randn((n_chunks, B, N, H, D), generator=g, device=dev)
+    if interleaved:
+        o = torch.randn((B, N, H, n_chunks, D), generator=g, device=dev).permute(3, 0, 1, 2, 4)
+    else:
+        o = torch.randn((n_chunks, B, N, H, D), generator=g, device=dev)
     l = torch.randn((n_chunks, B, H, N), generator=g, device=dev) + 10.0
     out = torch.empty((B, N, H, D), device=dev)
     lo = torch.empty((B, H, N), device=dev)
@@ -460,9 +466,10 @@ def main(argv=None):
     if lay is not None:
         gbs = lay[0] / (lay[1] * 1e-3) / 1e9
         extra["layout"] = {"bytes": lay[0], "ms": lay[1], "GB/s": gbs, "frac_hbm": gbs / float(peaks["hbm_gbs"])}
-    mb, mms = time_merge_kernel(dev, w.B, w.N, w.H, w.D, n_chunks=9)
-    mgbs = mb / (mms * 1e-3) / 1e9
-    extra["merge_n9"] = {"bytes": mb, "ms": mms, "GB/s": mgbs, "frac_hbm": mgbs / float(peaks["hbm_gbs"])}
+    for il, key in ((True, "merge_n9_interleaved"), (False, "merge_n9_chunk_major")):
+        mb, mms = time_merge_kernel(dev, w.B, w.N, w.H, w.D, n_chunks=9, interleaved=il)
+        mgbs = mb / (mms * 1e-3) / 1e9
+        extra[key] = {"bytes": mb, "ms": mms, "GB/s": mgbs, "frac_hbm": mgbs / float(peaks["hbm_gbs"])}
 
     # ---------------- end-to-end through host buffers
     e2e = None

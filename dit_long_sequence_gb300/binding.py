@@ -42,7 +42,7 @@ _lib.dit_attn_fwd.restype = _i
 _lib.dit_attn_fwd.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
                               _vp, _i, _vp, _vp]
 _lib.dit_attn_lse_merge.restype = _i
-_lib.dit_attn_lse_merge.argtypes = [_vp, _i64, _vp, _i64, _i, _i, _i, _i, _i, _vp, _i, _vp, _vp]
+_lib.dit_attn_lse_merge.argtypes = [_vp, _i64, _i64, _vp, _i64, _i, _i, _i, _i, _i, _vp, _i, _vp, _vp]
 _lib.dit_qkv_to_head_major.restype = _i
 _lib.dit_qkv_to_head_major.argtypes = [_vp, _i64, _i64, _i, _i, _i, _i, _vp, _vp, _vp, _vp]
 _lib.dit_status_string.restype = ctypes.c_char_p
@@ -116,23 +116,32 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, key_valid_len
 
 def lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, *, out: torch.Tensor | None = None,
               lse_out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32, stream=None):
-    """Merge n partials: o_parts [n, B, Nq, H, D] fp32, lse_parts [n, B, H, Nq] fp32
-    (each chunk contiguous; chunks may be strided).  Returns (out, lse_out)."""
+    """Merge n partials through `dit_attn_lse_merge`.
+
+    o_parts [n, B, Nq, H, D] fp32: any view whose (B, Nq, H) dims collapse to one
+    row index with a common row stride and d contiguous -- chunk-major
+    (contiguous [n, B, Nq, H, D]) or interleaved (a [B, Nq, H, n, D] buffer seen
+    through .permute(3, 0, 1, 2, 4)); lse_parts [n, B, H, Nq] fp32 with every
+    chunk contiguous.  Returns (out [B, Nq, H, D], lse_out [B, H, Nq]).
+    """
     n, B, Nq, H, D = o_parts.shape
     if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
         raise TypeError("partials must be fp32")
     if tuple(lse_parts.shape) != (n, B, H, Nq):
         raise ValueError("lse_parts must be [n, B, H, Nq]")
-    if not o_parts[0].is_contiguous() or not lse_parts[0].is_contiguous():
-        raise ValueError("each chunk must be contiguous")
+    rs = o_parts.stride(3)
+    if o_parts.stride(4) != 1 or o_parts.stride(2) != H * rs or o_parts.stride(1) != Nq * H * rs:
+        raise ValueError("o_parts rows must share one stride with d contiguous")
+    if not lse_parts[0].is_contiguous():
+        raise ValueError("each LSE chunk must be contiguous")
     if out is None:
         out = torch.empty((B, Nq, H, D), dtype=out_dtype, device=o_parts.device)
     if lse_out is None:
         lse_out = torch.empty((B, H, Nq), dtype=torch.float32, device=o_parts.device)
     if not out.is_contiguous() or not lse_out.is_contiguous():
         raise ValueError("outputs must be contiguous")
-    rc = _lib.dit_attn_lse_merge(o_parts.data_ptr(), o_parts.stride(0), lse_parts.data_ptr(), lse_parts.stride(0),
-                                 n, B, Nq, H, D, out.data_ptr(),
+    rc = _lib.dit_attn_lse_merge(o_parts.data_ptr(), o_parts.stride(0), rs, lse_parts.data_ptr(),
+                                 lse_parts.stride(0), n, B, Nq, H, D, out.data_ptr(),
                                  DIT_F32 if out.dtype == torch.float32 else DIT_BF16, lse_out.data_ptr(),
                                  _stream_ptr(stream))
     _check(rc, "dit_attn_lse_merge")

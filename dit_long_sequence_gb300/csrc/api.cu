@@ -169,9 +169,9 @@ dit_status_t dit_attn_fwd(const void* q, const void* k, const void* v, const dit
     return e == cudaSuccess ? DIT_OK : DIT_ERR_CUDA;
 }
 
-dit_status_t dit_attn_lse_merge(const float* o_parts, int64_t o_chunk_stride, const float* lse_parts,
-                                int64_t lse_chunk_stride, int n_chunks, int B, int Nq, int H, int D, void* out,
-                                dit_dtype_t out_dtype, float* lse_out, dit_stream_t stream) {
+dit_status_t dit_attn_lse_merge(const float* o_parts, int64_t o_chunk_stride, int64_t o_row_stride,
+                                const float* lse_parts, int64_t lse_chunk_stride, int n_chunks, int B, int Nq, int H,
+                                int D, void* out, dit_dtype_t out_dtype, float* lse_out, dit_stream_t stream) {
     if (n_chunks < 1 || n_chunks > 64) return DIT_ERR_INVALID_ARG;
     if (B < 0 || Nq < 0 || H < 0) return DIT_ERR_INVALID_ARG;
     if (out_dtype != DIT_BF16 && out_dtype != DIT_F32) return DIT_ERR_INVALID_ARG;
@@ -179,17 +179,22 @@ dit_status_t dit_attn_lse_merge(const float* o_parts, int64_t o_chunk_stride, co
     if (B == 0 || Nq == 0 || H == 0) return DIT_OK;
     if (o_parts == nullptr || lse_parts == nullptr || out == nullptr) return DIT_ERR_INVALID_ARG;
     const int64_t rows = static_cast<int64_t>(B) * Nq * H;
+    if (o_row_stride < D || o_chunk_stride < 0 || lse_chunk_stride < 0) return DIT_ERR_INVALID_ARG;
     if (n_chunks > 1) {
-        if (o_chunk_stride < rows * D || lse_chunk_stride < rows) return DIT_ERR_INVALID_ARG;
+        // chunks must not overlap: either chunk-major or interleaved within a row
+        const bool chunk_major = o_chunk_stride >= (rows - 1) * o_row_stride + D;
+        const bool interleaved = o_chunk_stride >= D && o_row_stride >= n_chunks * o_chunk_stride;
+        if (!chunk_major && !interleaved) return DIT_ERR_INVALID_ARG;
+        if (lse_chunk_stride < rows) return DIT_ERR_INVALID_ARG;
     }
-    if (o_chunk_stride < 0 || lse_chunk_stride < 0) return DIT_ERR_INVALID_ARG;
-    if (o_chunk_stride % 4 != 0) return DIT_ERR_ALIGNMENT;
+    if (o_chunk_stride % 4 != 0 || o_row_stride % 4 != 0) return DIT_ERR_ALIGNMENT;
     if (!aligned16(o_parts) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse_parts) & 3u) ||
         (reinterpret_cast<uintptr_t>(lse_out) & 3u))
         return DIT_ERR_ALIGNMENT;
     MergeArgs a;
     a.o_parts = o_parts;
     a.o_chunk_stride = o_chunk_stride;
+    a.o_row_stride = o_row_stride;
     a.lse_parts = lse_parts;
     a.lse_chunk_stride = lse_chunk_stride;
     a.n_chunks = n_chunks;

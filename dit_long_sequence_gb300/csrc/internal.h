@@ -35,6 +35,7 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
 struct MergeArgs {
     const float* o_parts;
     int64_t o_chunk_stride;
+    int64_t o_row_stride;
     const float* lse_parts;
     int64_t lse_chunk_stride;
     int n_chunks;

@@ -8,10 +8,11 @@
 // source pitch is taken from the input stride, head and channel contiguous
 // within each sequence row.  Here the scatter target is this GPU's own HBM.
 //
-// Pure data movement, HBM-bound.  A CTA copies kRows consecutive sequence rows
-// of one batch entry: 16-byte loads walk each fused row contiguously, and for
-// every (t, h) plane the kRows destination rows form one contiguous run of
-// kRows * D * 2 bytes.  All loads of a thread are issued before its stores.
+// Pure data movement, HBM-bound.  One warp copies one run of 32 consecutive
+// sequence rows of one (b, t, h) plane: its stores form a single contiguous
+// 32 * D * 2-byte range of the destination, its loads 32 strided 2*D-byte
+// segments of the source; every lane keeps kUnroll 16-byte loads in flight
+// before it stores.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -22,49 +23,47 @@ namespace dit {
 namespace {
 
 constexpr int kLayoutThreads = 256;
-constexpr int kRows = 4;     // sequence rows per CTA step
-constexpr int kUnroll = 4;   // 16-byte vectors in flight per thread
+constexpr int kRunRows = 32;   // sequence rows per warp unit
+constexpr int kUnroll = 8;     // 16-byte vectors in flight per lane
 
 __global__ void __launch_bounds__(kLayoutThreads) qkv_layout_kernel(const LayoutArgs a) {
-    const int vec_per_d = a.D / 8;                    // 16-byte vectors per head row
-    const int vec_per_row = 3 * a.H * vec_per_d;      // per fused sequence row
-    const int64_t groups_per_b = (a.N + kRows - 1) / kRows;
-    const int64_t n_groups = groups_per_b * a.B;
-    const int items = kRows * vec_per_row;            // vectors per CTA step
-
-    for (int64_t g = blockIdx.x; g < n_groups; g += gridDim.x) {
-        const int64_t b = g / groups_per_b;
-        const int n0 = static_cast<int>(g - b * groups_per_b) * kRows;
-        const uint16_t* src_b = a.qkv + b * a.stride_b;
-        for (int base = threadIdx.x; base < items; base += kLayoutThreads * kUnroll) {
+    const int vec_per_d = a.D / 8;                 // 16-byte vectors per head row
+    const int64_t n_runs = (a.N + kRunRows - 1) / kRunRows;
+    const int planes = 3 * a.H;
+    const int64_t units = static_cast<int64_t>(a.B) * planes * n_runs;
+    const int lane = threadIdx.x & 31;
+    const int warps_per_block = kLayoutThreads / 32;
+    const int64_t w0 = static_cast<int64_t>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
+    const int64_t ws = static_cast<int64_t>(gridDim.x) * warps_per_block;
+    const int total = kRunRows * vec_per_d;        // vectors in one run
+    for (int64_t u = w0; u < units; u += ws) {
+        const int64_t run = u % n_runs;
+        const int64_t rest = u / n_runs;
+        const int p = static_cast<int>(rest % planes);   // p = t*H + h
+        const int64_t b = rest / planes;
+        const int t = p / a.H;
+        const int hh = p - t * a.H;
+        const int n0 = static_cast<int>(run * kRunRows);
+        const uint16_t* src = a.qkv + b * a.stride_b + static_cast<int64_t>(p) * a.D;
+        uint16_t* plane = t == 0 ? a.out[0] : (t == 1 ? a.out[1] : a.out[2]);
+        uint16_t* dst = plane + (b * a.H + hh) * static_cast<int64_t>(a.N) * a.D;
+        for (int base = lane; base < total; base += 32 * kUnroll) {
             uint4 v[kUnroll];
-            const uint16_t* dst[kUnroll];
+            int n[kUnroll], c[kUnroll];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int it = base + u * kLayoutThreads;
-                dst[u] = nullptr;
-                if (it < items) {
-                    // item -> (plane p = t*H + h, row r, vector c); plane-major so
-                    // that consecutive threads write one contiguous run per plane.
-                    const int per_plane = kRows * vec_per_d;
-                    const int p = it / per_plane;
-                    const int rem = it - p * per_plane;
-                    const int r = rem / vec_per_d;
-                    const int c = rem - r * vec_per_d;
-                    const int n = n0 + r;
-                    if (n < a.N) {
-                        const int t = p / a.H;
-                        const int hh = p - t * a.H;
-                        const uint16_t* src = src_b + static_cast<int64_t>(n) * a.stride_n +
-                                              static_cast<int64_t>(p) * a.D + c * 8;
-                        v[u] = __ldcs(reinterpret_cast<const uint4*>(src));
-                        dst[u] = a.out[t] + ((b * a.H + hh) * static_cast<int64_t>(a.N) + n) * a.D + c * 8;
-                    }
-                }
+            for (int k = 0; k < kUnroll; ++k) {
+                const int it = base + k * 32;
+                n[k] = n0 + it / vec_per_d;
+                c[k] = it - (it / vec_per_d) * vec_per_d;
+                if (it < total && n[k] < a.N)
+                    v[k] = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(n[k]) * a.stride_n + c[k] * 8));
+                else
+                    n[k] = -1;
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u)
-                if (dst[u] != nullptr) __stcs(reinterpret_cast<uint4*>(const_cast<uint16_t*>(dst[u])), v[u]);
+            for (int k = 0; k < kUnroll; ++k)
+                if (n[k] >= 0)
+                    __stcs(reinterpret_cast<uint4*>(dst + static_cast<int64_t>(n[k]) * a.D + c[k] * 8), v[k]);
         }
     }
 }
@@ -75,9 +74,10 @@ cudaError_t launch_qkv_to_head_major(const LayoutArgs& a, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const int64_t n_groups = static_cast<int64_t>((a.N + kRows - 1) / kRows) * a.B;
+    const int64_t units = static_cast<int64_t>(a.B) * 3 * a.H * ((a.N + kRunRows - 1) / kRunRows);
     int64_t blocks = static_cast<int64_t>(device_sm_count(dev)) * 8;
-    if (blocks > n_groups) blocks = n_groups;
+    const int64_t need = (units + kLayoutThreads / 32 - 1) / (kLayoutThreads / 32);
+    if (blocks > need) blocks = need;
     if (blocks < 1) blocks = 1;
     qkv_layout_kernel<<<static_cast<unsigned>(blocks), kLayoutThreads, 0, stream>>>(a);
     return cudaGetLastError();

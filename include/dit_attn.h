@@ -109,15 +109,21 @@ dit_status_t dit_attn_fwd(const void *q, const void *k, const void *v,
  *   LSE = M + ln sum_k w_k.  Chunks with LSE_k = -inf get weight 0 (their O_k
  *   is not read); a row whose chunks are all -inf yields O = 0, LSE = -inf.
  *
- * o_parts    fp32, chunk k row (b, i, h) at o_parts + k*o_chunk_stride +
- *            ((b*Nq + i)*H + h)*D  (each chunk a contiguous [B, Nq, H, D]).
+ * o_parts    fp32, chunk k, row (b, i, h), channel d at
+ *              o_parts + k*o_chunk_stride + ((b*Nq + i)*H + h)*o_row_stride + d.
+ *            o_row_stride = D with o_chunk_stride = B*Nq*H*D is the chunk-major
+ *            layout [n, B, Nq, H, D]; o_row_stride = n*D with o_chunk_stride = D
+ *            interleaves the chunks per row ([B, Nq, H, n, D]), which the kernel
+ *            reads as one contiguous stream (dit_attn_fwd can write either
+ *            through its output strides).  Strides multiples of 4, chunks must
+ *            not overlap.
  * lse_parts  fp32, chunk k at lse_parts + k*lse_chunk_stride, [B, H, Nq] contiguous.
- * n_chunks in [1, 64]; D in {64, 128}.  o_chunk_stride a multiple of 4 elements.
+ * n_chunks in [1, 64]; D in {64, 128}.
  * out        [B, Nq, H, D] contiguous, out_dtype DIT_F32 or DIT_BF16.
  * lse_out    fp32 [B, H, Nq] contiguous, may be NULL.
  * All pointers 16-byte aligned.  Output must not overlap any input.
  */
-dit_status_t dit_attn_lse_merge(const float *o_parts, int64_t o_chunk_stride,
+dit_status_t dit_attn_lse_merge(const float *o_parts, int64_t o_chunk_stride, int64_t o_row_stride,
                                 const float *lse_parts, int64_t lse_chunk_stride,
                                 int n_chunks, int B, int Nq, int H, int D,
                                 void *out, dit_dtype_t out_dtype, float *lse_out,

@@ -83,11 +83,11 @@ def test_attn_fwd_argument_checks(lib):
 
 def test_merge_argument_checks(lib):
     f = lib.raw().dit_attn_lse_merge
-    ok_args = (FAKE, 1 * 8 * 4 * 128, FAKE, 1 * 4 * 8, 2, 1, 8, 4, 128, FAKE, lib.DIT_F32, FAKE, None)
+    ok_args = (FAKE, 1 * 8 * 4 * 128, 128, FAKE, 1 * 4 * 8, 2, 1, 8, 4, 128, FAKE, lib.DIT_F32, FAKE, None)
 
     def call(**kw):
         a = list(ok_args)
-        names = ["o", "ocs", "l", "lcs", "n", "B", "Nq", "H", "D", "out", "dt", "lo", "s"]
+        names = ["o", "ocs", "ors", "l", "lcs", "n", "B", "Nq", "H", "D", "out", "dt", "lo", "s"]
         for k_, v_ in kw.items():
             a[names.index(k_)] = v_
         return f(*a)
@@ -95,6 +95,9 @@ def test_merge_argument_checks(lib):
     assert call(n=65) == lib.DIT_ERR_INVALID_ARG
     assert call(D=32) == lib.DIT_ERR_UNSUPPORTED
     assert call(ocs=8) == lib.DIT_ERR_INVALID_ARG      # chunks would overlap
+    assert call(ocs=64, ors=256) == lib.DIT_ERR_INVALID_ARG   # interleaved chunks overlap within a row
+    assert call(ors=64) == lib.DIT_ERR_INVALID_ARG     # row stride below D
+    assert call(ocs=100000, ors=130) == lib.DIT_ERR_ALIGNMENT
     assert call(o=None) == lib.DIT_ERR_INVALID_ARG
     assert call(o=FAKE + 4) == lib.DIT_ERR_ALIGNMENT
     assert call(B=0) == lib.DIT_OK

@@ -57,6 +57,21 @@ def test_merge_matches_oracle(n, B, Nq, H, D):
     assert torch.equal(L, Lb)
 
 
+@pytest.mark.parametrize("n,B,Nq,H,D", [(9, 1, 200, 4, 128), (3, 2, 130, 3, 64)])
+def test_merge_interleaved_layout(n, B, Nq, H, D):
+    # chunks interleaved per row: a [B, Nq, H, n, D] buffer seen as [n, B, Nq, H, D]
+    o, l = _partials(n, B, Nq, H, D, seed=50 + n)
+    buf = o.permute(1, 2, 3, 0, 4).contiguous()
+    o_il = buf.permute(3, 0, 1, 2, 4)
+    assert o_il.stride(3) == n * D and o_il.stride(0) == D
+    O, L = _dl().lse_merge(o_il, l)
+    O2, L2 = _dl().lse_merge(o, l)
+    torch.cuda.synchronize()
+    Or, Lr = oracle.lse_merge(o.double().cpu().numpy(), l.double().cpu().numpy())
+    assert torch.equal(O, O2) and torch.equal(L, L2), "layouts disagree"
+    assert np.abs(O.double().cpu().numpy() - Or).max() <= 1e-5
+
+
 def test_chunked_attention_merge_equals_single_pass():
     B, N, H, D = 1, 900, 2, 128
     q, k, v, _ = wl.make_qkv(B, N, H, D, seed=30, device=_dev())
@@ -77,16 +92,19 @@ def test_chunked_attention_merge_equals_single_pass():
 
 
 def test_ring9_workload_chunked_vs_oracle_and_single_pass():
+    # the attention writes each chunk's O straight into a per-row interleaved
+    # [B, N, H, n, D] buffer through its output strides; the merge reads it back
     w = wl.WORKLOADS["ring9"]
     q, k, v, _ = wl.make_workload_inputs(w, device=_dev())
     n = w.kv_chunks
     cl = w.N // n
-    o_parts = torch.empty(n, w.B, w.N, w.H, w.D, device=_dev())
+    o_buf = torch.empty(w.B, w.N, w.H, n, w.D, device=_dev())
     l_parts = torch.empty(n, w.B, w.H, w.N, device=_dev())
     for c in range(n):
-        _dl().attn_fwd(q, k[:, c * cl:(c + 1) * cl], v[:, c * cl:(c + 1) * cl], out=o_parts[c], lse=l_parts[c])
-    O, L = _dl().lse_merge(o_parts, l_parts)
-    del o_parts, l_parts
+        _dl().attn_fwd(q, k[:, c * cl:(c + 1) * cl], v[:, c * cl:(c + 1) * cl], out=o_buf[:, :, :, c],
+                       lse=l_parts[c])
+    O, L = _dl().lse_merge(o_buf.permute(3, 0, 1, 2, 4), l_parts)
+    del o_buf, l_parts
     O1, L1 = _dl().attn_fwd(q, k, v)
     torch.cuda.synchronize()
     assert (O - O1).abs().max().item() <= 2e-3
