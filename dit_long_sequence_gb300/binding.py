@@ -41,6 +41,11 @@ _vp, _i, _i64, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_floa
 _lib.dit_attn_fwd.restype = _i
 _lib.dit_attn_fwd.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
                               _vp, _i, _vp, _vp]
+_lib.dit_attn_fwd_accumulate.restype = _i
+_lib.dit_attn_fwd_accumulate.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
+                                         _vp, _vp, _vp]
+_lib.dit_watchdog_selftest.restype = _i
+_lib.dit_watchdog_selftest.argtypes = [ctypes.c_uint32, _vp]
 _lib.dit_attn_lse_merge.restype = _i
 _lib.dit_attn_lse_merge.argtypes = [_vp, _i64, _i64, _vp, _i64, _i, _i, _i, _i, _i, _vp, _i, _vp, _vp]
 _lib.dit_qkv_to_head_major.restype = _i
@@ -51,8 +56,8 @@ _lib.dit_check_watchdog.restype = _i
 _lib.dit_check_watchdog.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
 _lib.dit_version.restype = ctypes.c_uint32
 
-EXPORTS = ("dit_attn_fwd", "dit_attn_lse_merge", "dit_qkv_to_head_major", "dit_status_string",
-           "dit_check_watchdog", "dit_version")
+EXPORTS = ("dit_attn_fwd", "dit_attn_fwd_accumulate", "dit_attn_lse_merge", "dit_qkv_to_head_major",
+           "dit_status_string", "dit_check_watchdog", "dit_watchdog_selftest", "dit_version")
 
 
 class DitError(RuntimeError):
@@ -114,6 +119,30 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, key_valid_len
     return out, lse
 
 
+def attn_fwd_accumulate(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor, *,
+                        key_valid_len: int | None = None, scale: float | None = None, stream=None):
+    """Fold attention of q over this key chunk into the running fp32 (out, lse)
+    in place, through `dit_attn_fwd_accumulate`.  Start from lse = -inf."""
+    B, Nq, H, D = q.shape
+    Nkv = k.shape[1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a bf16 CUDA tensor")
+    if k.shape != (B, Nkv, H, D) or v.shape != (B, Nkv, H, D):
+        raise ValueError("k and v must be [B, Nkv, H, D] matching q")
+    if out.dtype != torch.float32 or tuple(out.shape) != (B, Nq, H, D):
+        raise ValueError("out must be an fp32 [B, Nq, H, D] tensor")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
+    kvl = Nkv if key_valid_len is None else int(key_valid_len)
+    sc = float(D) ** -0.5 if scale is None else float(scale)
+    st = AttnStrides(_strides4(q), _strides4(k), _strides4(v), _strides4(out))
+    rc = _lib.dit_attn_fwd_accumulate(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(st), B, Nq, Nkv, H, D,
+                                      kvl, sc, out.data_ptr(), lse.data_ptr(), _stream_ptr(stream))
+    _check(rc, "dit_attn_fwd_accumulate")
+    return out, lse
+
+
 def lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, *, out: torch.Tensor | None = None,
               lse_out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32, stream=None):
     """Merge n partials through `dit_attn_lse_merge`.
@@ -166,6 +195,12 @@ def qkv_to_head_major(qkv: torch.Tensor, *, outs=None, stream=None):
                                     _stream_ptr(stream))
     _check(rc, "dit_qkv_to_head_major")
     return outs
+
+
+def watchdog_selftest(limit_us: int = 100_000, stream=None):
+    """Enqueue the library's watchdog self-test (a bounded wait that must run
+    out); read the outcome with check_watchdog()."""
+    _check(_lib.dit_watchdog_selftest(int(limit_us), _stream_ptr(stream)), "dit_watchdog_selftest")
 
 
 def check_watchdog(stream=None):

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libditattn.so")
-SOURCES = ["api.cu", "attn_fwd.cu", "lse_merge.cu", "qkv_layout.cu"]
+SOURCES = ["api.cu", "attn_fwd.cu", "lse_merge.cu", "qkv_layout.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

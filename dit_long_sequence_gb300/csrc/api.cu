@@ -111,9 +111,13 @@ using namespace dit;
 
 extern "C" {
 
-dit_status_t dit_attn_fwd(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides, int B,
-                          int Nq, int Nkv, int H, int D, int key_valid_len, float scale, void* out,
-                          dit_dtype_t out_dtype, float* lse, dit_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides, int B,
+                             int Nq, int Nkv, int H, int D, int key_valid_len, float scale, void* out,
+                             dit_dtype_t out_dtype, float* lse, bool accumulate, dit_stream_t stream) {
     if (strides == nullptr) return DIT_ERR_INVALID_ARG;
     if (B < 0 || Nq < 0 || Nkv < 0 || H < 0) return DIT_ERR_INVALID_ARG;
     if (key_valid_len < 0 || key_valid_len > Nkv) return DIT_ERR_INVALID_ARG;
@@ -165,8 +169,27 @@ dit_status_t dit_attn_fwd(const void* q, const void* k, const void* v, const dit
     a.status = status_word(dev);
     a.timeout_ns = kWatchdogNs;
     if (a.status == nullptr) return DIT_ERR_CUDA;
-    cudaError_t e = launch_attn_fwd(tq, tk, tv, a, B, D, out_dtype == DIT_BF16, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_attn_fwd(tq, tk, tv, a, B, D, out_dtype == DIT_BF16, accumulate,
+                                    reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DIT_OK : DIT_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+dit_status_t dit_attn_fwd(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides, int B,
+                          int Nq, int Nkv, int H, int D, int key_valid_len, float scale, void* out,
+                          dit_dtype_t out_dtype, float* lse, dit_stream_t stream) {
+    return attn_fwd_common(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, scale, out, out_dtype, lse, false,
+                           stream);
+}
+
+dit_status_t dit_attn_fwd_accumulate(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides,
+                                     int B, int Nq, int Nkv, int H, int D, int key_valid_len, float scale, float* out,
+                                     float* lse, dit_stream_t stream) {
+    return attn_fwd_common(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, scale, out, DIT_F32, lse, true,
+                           stream);
 }
 
 dit_status_t dit_attn_lse_merge(const float* o_parts, int64_t o_chunk_stride, int64_t o_row_stride,
@@ -242,6 +265,16 @@ const char* dit_status_string(dit_status_t s) {
         case DIT_ERR_TIMEOUT: return "DIT_ERR_TIMEOUT: a bounded in-kernel wait ran out";
     }
     return "unknown dit_status_t";
+}
+
+dit_status_t dit_watchdog_selftest(uint32_t limit_us, dit_stream_t stream) {
+    if (limit_us < 1000 || limit_us > 2000000) return DIT_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DIT_ERR_CUDA;
+    unsigned int* st = status_word(dev);
+    if (st == nullptr) return DIT_ERR_CUDA;
+    cudaError_t e = launch_watchdog_selftest(st, 1000ull * limit_us, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DIT_OK : DIT_ERR_CUDA;
 }
 
 dit_status_t dit_check_watchdog(dit_stream_t stream, uint32_t info[4]) {

@@ -79,7 +79,9 @@ struct Cfg {
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
-template <int D, bool OUT_BF16>
+// ACCUM: fold this pass into an existing fp32 (O, LSE) pair instead of
+// overwriting it (streaming merge over key chunks).
+template <int D, bool OUT_BF16, bool ACCUM>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
@@ -387,16 +389,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) tc_fence_after();
         }
         if (ok) {
+            static_assert(!(ACCUM && OUT_BF16), "accumulation keeps O in fp32");
             const bool in_range = row < a.Nq;
             const int64_t o_off = static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(row) * a.o_sn +
                                   static_cast<int64_t>(h) * a.o_sh;
-            const float inv_l = n_tiles > 0 ? 1.f / l : 0.f;
+            const int64_t lse_idx = (static_cast<int64_t>(b) * a.H + h) * a.Nq + row;
+            const float lse_new = n_tiles > 0 ? (m + log2f(l)) * kLn2 : -INFINITY;
+            // out = c_prev * O_prev + c_new * O_tmem
+            float c_new = n_tiles > 0 ? 1.f / l : 0.f;
+            float c_prev = 0.f;
+            float lse_out = lse_new;
+            if constexpr (ACCUM) {
+                // Merge with the pass already in (out, lse): the same combine as
+                // dit_attn_lse_merge, for two partials.
+                const float lse_prev = in_range ? a.lse[lse_idx] : -INFINITY;
+                const float mx = fmaxf(lse_prev, lse_new);
+                if (mx == -INFINITY) {
+                    c_new = 0.f;
+                    lse_out = -INFINITY;
+                } else {
+                    const float wp = expf(lse_prev - mx);
+                    const float wn = expf(lse_new - mx);
+                    const float inv = 1.f / (wp + wn);
+                    c_prev = wp * inv;
+                    c_new = n_tiles > 0 ? wn * inv / l : 0.f;
+                    lse_out = mx + logf(wp + wn);
+                }
+            }
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
                 if (n_tiles > 0) {
                     tmem_ld32(tO + cc * 32, o);
-                    tmem_ld_wait();
+                    tmem_ld_wait_dep(o);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = 0u;
@@ -407,25 +432,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int v4 = 0; v4 < 4; ++v4) {
                             uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv_l, __uint_as_float(o[8 * v4 + 1]) * inv_l);
-                            w.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv_l, __uint_as_float(o[8 * v4 + 3]) * inv_l);
-                            w.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv_l, __uint_as_float(o[8 * v4 + 5]) * inv_l);
-                            w.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv_l, __uint_as_float(o[8 * v4 + 7]) * inv_l);
+                            w.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * c_new, __uint_as_float(o[8 * v4 + 1]) * c_new);
+                            w.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * c_new, __uint_as_float(o[8 * v4 + 3]) * c_new);
+                            w.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * c_new, __uint_as_float(o[8 * v4 + 5]) * c_new);
+                            w.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * c_new, __uint_as_float(o[8 * v4 + 7]) * c_new);
                             dst[v4] = w;
                         }
                     } else {
                         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + o_off + cc * 32);
 #pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
-                            dst[v4] = make_float4(__uint_as_float(o[4 * v4 + 0]) * inv_l, __uint_as_float(o[4 * v4 + 1]) * inv_l,
-                                                  __uint_as_float(o[4 * v4 + 2]) * inv_l, __uint_as_float(o[4 * v4 + 3]) * inv_l);
+                        for (int v4 = 0; v4 < 8; ++v4) {
+                            float4 r = make_float4(__uint_as_float(o[4 * v4 + 0]) * c_new, __uint_as_float(o[4 * v4 + 1]) * c_new,
+                                                   __uint_as_float(o[4 * v4 + 2]) * c_new, __uint_as_float(o[4 * v4 + 3]) * c_new);
+                            if (ACCUM && c_prev > 0.f) {
+                                const float4 pv = dst[v4];
+                                r.x = fmaf(c_prev, pv.x, r.x);
+                                r.y = fmaf(c_prev, pv.y, r.y);
+                                r.z = fmaf(c_prev, pv.z, r.z);
+                                r.w = fmaf(c_prev, pv.w, r.w);
+                            }
+                            dst[v4] = r;
+                        }
                     }
                 }
             }
-            if (in_range) {
-                const float lse = n_tiles > 0 ? (m + log2f(l)) * kLn2 : -INFINITY;
-                a.lse[(static_cast<int64_t>(b) * a.H + h) * a.Nq + row] = lse;
-            }
+            if (in_range) a.lse[lse_idx] = lse_out;
         }
     }
 
@@ -437,10 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool ACCUM>
 cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& args,
                         int B, cudaStream_t stream) {
-    auto kern = attn_fwd_kernel<D, BF16>;
+    auto kern = attn_fwd_kernel<D, BF16, ACCUM>;
     const int smem = Cfg<D>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -452,11 +483,16 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 }  // namespace
 
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const AttnArgs& args, int B, int D, bool out_bf16, cudaStream_t stream) {
-    if (D == 128) return out_bf16 ? launch_impl<128, true>(tq, tk, tv, args, B, stream)
-                                  : launch_impl<128, false>(tq, tk, tv, args, B, stream);
-    return out_bf16 ? launch_impl<64, true>(tq, tk, tv, args, B, stream)
-                    : launch_impl<64, false>(tq, tk, tv, args, B, stream);
+                            const AttnArgs& args, int B, int D, bool out_bf16, bool accumulate, cudaStream_t stream) {
+    if (accumulate) {
+        if (out_bf16) return cudaErrorInvalidValue;
+        return D == 128 ? launch_impl<128, false, true>(tq, tk, tv, args, B, stream)
+                        : launch_impl<64, false, true>(tq, tk, tv, args, B, stream);
+    }
+    if (D == 128) return out_bf16 ? launch_impl<128, true, false>(tq, tk, tv, args, B, stream)
+                                  : launch_impl<128, false, false>(tq, tk, tv, args, B, stream);
+    return out_bf16 ? launch_impl<64, true, false>(tq, tk, tv, args, B, stream)
+                    : launch_impl<64, false, false>(tq, tk, tv, args, B, stream);
 }
 
 }  // namespace dit

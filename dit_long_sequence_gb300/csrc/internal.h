@@ -28,9 +28,13 @@ struct AttnArgs {
     unsigned long long timeout_ns;
 };
 
-// Attention forward.  grid = (ceil(Nq/256), H, B), 320 threads.
+// Attention forward.  grid = (ceil(Nq/256), H, B), 384 threads.  accumulate:
+// merge into the fp32 (out, lse) already there instead of overwriting them.
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const AttnArgs& args, int B, int D, bool out_bf16, cudaStream_t stream);
+                            const AttnArgs& args, int B, int D, bool out_bf16, bool accumulate, cudaStream_t stream);
+
+// Watchdog self-test: one CTA waits on a barrier nothing arrives on.
+cudaError_t launch_watchdog_selftest(unsigned int* status, unsigned long long limit_ns, cudaStream_t stream);
 
 struct MergeArgs {
     const float* o_parts;

@@ -33,7 +33,7 @@ constexpr int kMaxChunks = 64;
 constexpr int kGroup = 16;  // chunk loads in flight per lane and row
 
 template <int D, bool OUT_BF16>
-__global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergeArgs a, int64_t n_pos) {
+__global__ void __launch_bounds__(kMergeThreads, 4) lse_merge_kernel(const MergeArgs a, int64_t n_pos) {
     constexpr int LPR = D / 4;    // lanes per row
     constexpr int RPW = 32 / LPR; // rows per warp step
     // weights of 32 heads x up to kMaxChunks chunks, per warp (0 = chunk skipped)

@@ -98,6 +98,29 @@ dit_status_t dit_attn_fwd(const void *q, const void *k, const void *v,
                           dit_stream_t stream);
 
 /*
+ * dit_attn_fwd_accumulate -- one more key chunk folded into a running result.
+ *
+ * The streaming form of the merge: "Scaling Video Generation Across NVL72 rack
+ * with TensorRT-LLM", "Ring Attention", paragraph "Online-softmax merge" (each
+ * ring step's partial output and LSE are merged into the running output in
+ * fp32, block by block, until it equals one global pass) and the "Difference
+ * from Ring" table of "Attention2D Parallelism" (streaming merge after every
+ * step, in place on the local rank).  Computes this call's (O_c, LSE_c) exactly
+ * as dit_attn_fwd and replaces the fp32 (out, lse) already in memory by
+ *   M = max(LSE, LSE_c),  w = exp(LSE - M),  w_c = exp(LSE_c - M),
+ *   out = (w out + w_c O_c) / (w + w_c),  lse = M + ln(w + w_c),
+ * so a sequence of calls over disjoint key chunks ends at the single-pass
+ * result.  Start from lse = -inf everywhere: rows whose lse is -inf take this
+ * call's result and their old `out` is not read (it may hold any bits).
+ * Arguments as dit_attn_fwd; `out` is fp32 only and is read and written.
+ */
+dit_status_t dit_attn_fwd_accumulate(const void *q, const void *k, const void *v,
+                                     const dit_attn_strides_t *strides,
+                                     int B, int Nq, int Nkv, int H, int D,
+                                     int key_valid_len, float scale,
+                                     float *out, float *lse, dit_stream_t stream);
+
+/*
  * dit_attn_lse_merge -- combine n_chunks partial (O_k, LSE_k) computed for the
  * same queries over disjoint key spans into the single-pass result.
  *
@@ -161,6 +184,16 @@ const char *dit_status_string(dit_status_t s);
  * code, block index, warp role, wait site) or DIT_ERR_CUDA.
  */
 dit_status_t dit_check_watchdog(dit_stream_t stream, uint32_t info[4]);
+
+/*
+ * dit_watchdog_selftest -- library self-test of the failure path; the pages
+ * have no counterpart.  Launches one CTA whose bounded wait can never be
+ * satisfied, so it gives up after `limit_us` microseconds (1,000 to 2,000,000),
+ * records DIT_ERR_TIMEOUT in the device status word (wait site 99) and exits
+ * normally; the CUDA context stays usable.  Read the result with
+ * dit_check_watchdog().  Returns DIT_OK once enqueued.
+ */
+dit_status_t dit_watchdog_selftest(uint32_t limit_us, dit_stream_t stream);
 
 /* Library version, (major << 16) | minor. */
 uint32_t dit_version(void);

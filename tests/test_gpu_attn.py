@@ -146,3 +146,39 @@ def _sampled_check(w, rows_per_head=1024):
 @pytest.mark.parametrize("name", ["ltx2_padded", "cosmos3_nano", "wan22_a14b"])
 def test_workload_sampled_rows(name):
     _sampled_check(wl.WORKLOADS[name])
+
+
+# ---------------------------------------------------- streaming accumulation
+
+@pytest.mark.parametrize("bounds,D", [([0, 100, 257, 300, 512, 700], 128), ([0, 128, 129, 400], 64)])
+def test_accumulate_over_key_chunks_equals_single_pass(bounds, D):
+    import dit_long_sequence_gb300 as dl
+    B, N, H = 1, 700 if D == 128 else 400, 2
+    q, k, v, _ = wl.make_qkv(B, N, H, D, seed=15, device=_dev())
+    out = torch.full((B, N, H, D), float("nan"), device=_dev())   # never read while lse = -inf
+    lse = torch.full((B, H, N), float("-inf"), device=_dev())
+    for lo, hi in zip(bounds[:-1], bounds[1:]):
+        dl.attn_fwd_accumulate(q, k[:, lo:hi], v[:, lo:hi], out, lse)
+    dl.attn_fwd_accumulate(q, k[:, :0], v[:, :0], out, lse)          # an empty chunk changes nothing
+    O1, L1 = _attn(q, k, v)
+    torch.cuda.synchronize()
+    assert (out - O1).abs().max().item() <= 2e-3
+    assert (lse - L1).abs().max().item() <= 1e-4
+    Or, Lr = parity.oracle_full(q, k, v)
+    parity.compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), Or, Lr, head_axes=(0, 2))
+
+
+def test_accumulate_ring_workload_sampled():
+    import dit_long_sequence_gb300 as dl
+    w = wl.WORKLOADS["ring9"]
+    q, k, v, _ = wl.make_workload_inputs(w, device=_dev())
+    cl = w.N // w.kv_chunks
+    out = torch.empty(w.B, w.N, w.H, w.D, device=_dev())
+    lse = torch.full((w.B, w.H, w.N), float("-inf"), device=_dev())
+    for c in range(w.kv_chunks):
+        dl.attn_fwd_accumulate(q, k[:, c * cl:(c + 1) * cl], v[:, c * cl:(c + 1) * cl], out, lse)
+    torch.cuda.synchronize()
+    rows = wl.sample_rows(w.B, w.H, w.N, 1024, seed=w.seed, must=[cl - 1, cl, w.N - 1])
+    Og, Lg = parity.gather_rows(out, lse, rows)
+    Or, Lr = parity.oracle_rows(q, k, v, rows)
+    parity.compare(Og, Lg, Or, Lr, head_axes=(0, 1))
