@@ -191,72 +191,79 @@ class Step:
         self.w, self.dev, self.dl = w, dev, dl
         self.stream = torch.cuda.current_stream(dev)
         B, N, H, D = w.B, w.N, w.H, w.D
-        self.mode = "layout+attn" if w.name.split("_h")[0] in ("ltx2_padded", "tiny") else (
+        base = w.name.split("_h")[0]
+        self.mode = "layout+attn" if base in ("ltx2_padded", "tiny") else (
             "chunked+merge" if w.kv_chunks > 1 else "attn")
         if self.mode == "layout+attn" or w.fused:
-            self.fused = wl.randn_bf16((B, N, 3, H, D), w.seed, dev)
-            self.q = self.k = self.v = None
-            if self.mode == "layout+attn":
-                self.planes = tuple(torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev) for _ in range(3))
-                self.q, self.k, self.v = (p.permute(0, 2, 1, 3) for p in self.planes)   # [B,N,H,D] views
-            else:
-                self.q, self.k, self.v = self.fused[:, :, 0], self.fused[:, :, 1], self.fused[:, :, 2]
+            # one fused [B, N, 3, H, D] projection buffer is the step's input
+            self.inputs = [wl.randn_bf16((B, N, 3, H, D), w.seed, dev)]
         else:
-            self.fused = None
-            self.q, self.k, self.v, _ = wl.make_qkv(B, N, H, D, w.seed, device=dev)
-        self.out = torch.empty((B, N, H, D), dtype=torch.float32, device=dev)
-        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+            q, k, v, _ = wl.make_qkv(B, N, H, D, w.seed, device=dev)
+            self.inputs = [q, k, v]
+        if self.mode == "layout+attn":
+            self.planes = tuple(torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev) for _ in range(3))
         if self.mode == "chunked+merge":
             n = w.kv_chunks
             # per-row interleaved partials [B, N, H, n, D]: the merge reads one stream
             self.o_buf = torch.empty((B, N, H, n, D), dtype=torch.float32, device=dev)
             self.o_parts = self.o_buf.permute(3, 0, 1, 2, 4)
             self.l_parts = torch.empty((n, B, H, N), dtype=torch.float32, device=dev)
+        self.out = torch.empty((B, N, H, D), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         self.launches_per_step = {"layout+attn": 2, "attn": 1, "chunked+merge": w.kv_chunks + 1}[self.mode]
         self.attn_events = []
 
-    def input_tensor(self):
-        """The tensor a user uploads per step (for the e2e leg)."""
-        if self.fused is not None:
-            return self.fused
-        return None
+    def qkv_of(self, inputs):
+        """The [B, N, H, D] q, k, v views the attention reads for these inputs."""
+        if self.mode == "layout+attn":
+            return tuple(p.permute(0, 2, 1, 3) for p in self.planes)
+        if len(inputs) == 1:
+            f = inputs[0]
+            return f[:, :, 0], f[:, :, 1], f[:, :, 2]
+        return tuple(inputs)
 
-    def run(self, record=False):
+    @property
+    def q(self):
+        return self.qkv_of(self.inputs)[0]
+
+    @property
+    def k(self):
+        return self.qkv_of(self.inputs)[1]
+
+    @property
+    def v(self):
+        return self.qkv_of(self.inputs)[2]
+
+    def launch(self, inputs, out, lse, stream, record=False):
+        """Enqueue one step reading `inputs` and writing (out, lse) on `stream`."""
         import torch
         dl, w = self.dl, self.w
-        ev = None
         if self.mode == "layout+attn":
-            dl.qkv_to_head_major(self.fused, outs=self.planes, stream=self.stream)
-            if record:
-                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                ev[0].record(self.stream)
-            dl.attn_fwd(self.q, self.k, self.v, key_valid_len=w.key_valid_len, out=self.out, lse=self.lse,
-                        stream=self.stream)
-            if record:
-                ev[1].record(self.stream)
-                self.attn_events.append(ev)
-        elif self.mode == "attn":
-            if record:
-                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                ev[0].record(self.stream)
-            dl.attn_fwd(self.q, self.k, self.v, key_valid_len=w.key_valid_len, out=self.out, lse=self.lse,
-                        stream=self.stream)
-            if record:
-                ev[1].record(self.stream)
-                self.attn_events.append(ev)
-        else:
+            dl.qkv_to_head_major(inputs[0], outs=self.planes, stream=stream)
+        q, k, v = self.qkv_of(inputs)
+        ev = None
+        if record:
+            ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            ev[0].record(stream)
+        if self.mode == "chunked+merge":
             n = w.kv_chunks
             cl = w.N // n
-            if record:
-                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                ev[0].record(self.stream)
             for c in range(n):
-                dl.attn_fwd(self.q, self.k[:, c * cl:(c + 1) * cl], self.v[:, c * cl:(c + 1) * cl],
-                            out=self.o_parts[c], lse=self.l_parts[c], stream=self.stream)
-            if record:
-                ev[1].record(self.stream)
-                self.attn_events.append(ev)
-            dl.lse_merge(self.o_parts, self.l_parts, out=self.out, lse_out=self.lse, stream=self.stream)
+                dl.attn_fwd(q, k[:, c * cl:(c + 1) * cl], v[:, c * cl:(c + 1) * cl],
+                            out=self.o_parts[c], lse=self.l_parts[c], stream=stream)
+        else:
+            dl.attn_fwd(q, k, v, key_valid_len=w.key_valid_len, out=out, lse=lse, stream=stream)
+        if record:
+            ev[1].record(stream)
+            self.attn_events.append(ev)
+        if self.mode == "chunked+merge":
+            dl.lse_merge(self.o_parts, self.l_parts, out=out, lse_out=lse, stream=stream)
+
+    def run(self, record=False):
+        self.launch(self.inputs, self.out, self.lse, self.stream, record=record)
+
+    def input_tensor(self):
+        return self.inputs[0] if len(self.inputs) == 1 else None
 
     def attn_ms_per_launch(self):
         import torch
@@ -306,11 +313,11 @@ def time_layout_kernel(step, reps=5):
     for _ in range(reps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(s)
-        step.dl.qkv_to_head_major(step.fused, outs=step.planes, stream=s)
+        step.dl.qkv_to_head_major(step.inputs[0], outs=step.planes, stream=s)
         b.record(s)
         b.synchronize()
         ts.append(a.elapsed_time(b))
-    nbytes = 2 * step.fused.numel() * 2
+    nbytes = 2 * step.inputs[0].numel() * 2
     return nbytes, statistics.median(ts)
 
 
@@ -490,45 +497,66 @@ def main(argv=None):
 
 
 def run_e2e(step, args, world):
-    """Same metric through the C ABI with host buffers: per step, copy the inputs
-    from pinned host memory, run the step, copy O and LSE back."""
+    """Same metric through the C ABI with host buffers.  Every step copies its
+    inputs from pinned host memory, runs, and copies O and LSE back; copies run
+    on their own streams so that step i+1's upload and step i-1's download
+    overlap step i's kernels (two device buffer sets, ordered by events)."""
     import torch
-    src = step.input_tensor()
-    if src is not None:
-        host_in = [torch.empty(src.shape, dtype=src.dtype, pin_memory=True)]
-        dev_in = [src]
-    else:
-        host_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (step.q, step.k, step.v)]
-        dev_in = [step.q, step.k, step.v]
-    for h, d in zip(host_in, dev_in):
+    dev = step.dev
+    host_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in step.inputs]
+    for h, d in zip(host_in, step.inputs):
         h.copy_(d)
-    host_o = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
-    host_l = torch.empty(step.lse.shape, dtype=step.lse.dtype, pin_memory=True)
-    s = step.stream
+    dev_in = [step.inputs, [torch.empty_like(t) for t in step.inputs]]
+    dev_out = [(step.out, step.lse), (torch.empty_like(step.out), torch.empty_like(step.lse))]
+    host_out = [(torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True),
+                 torch.empty(step.lse.shape, dtype=step.lse.dtype, pin_memory=True)) for _ in range(2)]
+    s_comp = step.stream
+    s_h2d = torch.cuda.Stream(device=dev)
+    s_d2h = torch.cuda.Stream(device=dev)
 
-    def one():
-        for h, d in zip(host_in, dev_in):
-            d.copy_(h, non_blocking=True)
-        step.run()
-        host_o.copy_(step.out, non_blocking=True)
-        host_l.copy_(step.lse, non_blocking=True)
+    def pipeline(n_steps, t_start=None, t_end=None):
+        comp_done, d2h_done = {}, {}
+        if t_start is not None:
+            t_start.record(s_h2d)
+        for i in range(n_steps):
+            slot = i & 1
+            h2d_done = torch.cuda.Event()
+            with torch.cuda.stream(s_h2d):
+                if i >= 2:
+                    s_h2d.wait_event(comp_done[i - 2])      # the inputs of step i-2 were consumed
+                for h, d in zip(host_in, dev_in[slot]):
+                    d.copy_(h, non_blocking=True)
+                h2d_done.record(s_h2d)
+            s_comp.wait_event(h2d_done)
+            if i >= 2:
+                s_comp.wait_event(d2h_done[i - 2])          # step i-2's result has been read back
+            o, l = dev_out[slot]
+            step.launch(dev_in[slot], o, l, s_comp)
+            comp_done[i] = torch.cuda.Event()
+            comp_done[i].record(s_comp)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(comp_done[i])
+                host_out[slot][0].copy_(o, non_blocking=True)
+                host_out[slot][1].copy_(l, non_blocking=True)
+                d2h_done[i] = torch.cuda.Event()
+                d2h_done[i].record(s_d2h)
+        if t_end is not None:
+            s_d2h.wait_event(comp_done[n_steps - 1])
+            t_end.record(s_d2h)
 
-    for _ in range(3):
-        one()
+    pipeline(3)
     torch.cuda.synchronize()
     barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(s)
-    for _ in range(args.steps):
-        one()
-    b.record(s)
+    pipeline(args.steps, a, b)
     torch.cuda.synchronize()
     barrier()
     ms = reduce_max(a.elapsed_time(b))
     h2d = sum(h.numel() * h.element_size() for h in host_in)
-    d2h = host_o.numel() * host_o.element_size() + host_l.numel() * host_l.element_size()
+    d2h = host_out[0][0].numel() * host_out[0][0].element_size() + host_out[0][1].numel() * host_out[0][1].element_size()
     return {"value": world * step.w.flops() * args.steps / (ms * 1e-3) / 1e12, "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps,
+            "pipelined": "uploads and downloads on copy streams overlap the neighbouring steps' kernels"}
 
 
 if __name__ == "__main__":
