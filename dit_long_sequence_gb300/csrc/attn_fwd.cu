@@ -32,12 +32,13 @@
 //   which makes writing S_t(j+1) over P_t(j) safe after PV_t(j).
 //
 // Online softmax in log2 units with a lazy rescale: the running max m of a row
-// only moves (and O, l are rescaled by 2^(m_old - m_new)) when the tile max
-// exceeds m by more than 8; otherwise exponents use the stale m, so every P
-// stays <= 2^8 and the final O / l is exact because both use the same m.
-// Because the rescale is rare, the exponents of a tile are computed with the
-// running max while the tile max is still being formed; the few warps that do
-// need a rescale recompute that tile's P.
+// is set by the first key tile and only moves (O and l rescaled by
+// 2^(m_old - m_new)) when a later tile's row sum of 2^(s*sl2 - m) exceeds 2^39;
+// otherwise every P <= 2^39, which bf16 P and the fp32 accumulators carry with
+// unchanged relative precision, and the final O / l and LSE = ln2 * (m + log2 l)
+// are exact whatever m is.  So the steady state needs no per-tile row max at
+// all: the exponents are computed straight away and the already-needed row sum
+// doubles as the overflow check; the rare warps that fail it recompute P.
 //
 // Keys j >= kv_len are outside the K/V tensor maps (zero fill) and masked to
 // -inf in the last tile, so pad rows are never read.
@@ -57,7 +58,7 @@ constexpr uint32_t kSoftmaxRegs = 208;
 constexpr uint32_t kOtherRegs = 88;
 static_assert(256 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * 168, "register split");
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kSumLimit = 549755813888.0f;  // 2^39: largest tile row sum kept without a rescale
 
 template <int D>
 struct Cfg {
@@ -325,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 64; ++c)
                     if (c >= valid) s[c] = -INFINITY;
             }
-            const float mxA = max64(s);
             if (j == 0) {
+                const float mxA = max64(s);
                 // First tile: no running max yet, so take the tile max first.
                 tmem_ld_wait_dep(sr[2]);
                 reg_dep(sr[3]);
@@ -340,8 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m = fmaxf(mxA, max64(s + 64)) * sl2;
                 l = exp_store(s, tS, m) + exp_store(s + 64, tS + 32, m);
             } else {
-                // Exponents with the running max while the tile max is formed; a
-                // row whose max grew by more than the threshold redoes them below.
+                // Exponents with the running max m, no tile max: if the tile's row
+                // sum stays <= 2^39 then every P <= 2^39, which bf16 P and the fp32
+                // O / l accumulators hold exactly as well as P <= 1.  Rows whose sum
+                // exceeds it (their max grew by more than ~32 in log2 units) take
+                // the slow path: tile max, O rescale, P recomputed.
                 float lA = exp_store(s, tS, m);
                 tmem_ld_wait_dep(sr[2]);
                 reg_dep(sr[3]);
@@ -352,14 +356,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 64; c < 128; ++c)
                         if (c >= valid) s[c] = -INFINITY;
                 }
-                const float mxB = max64(s + 64);
                 float lB = exp_store(s + 64, tS + 32, m);
-                const float m_tile = fmaxf(mxA, mxB) * sl2;
-                const bool need = m_tile > m + kRescaleThreshold;
+                const bool need = !(lA + lB <= kSumLimit);   // also true for inf / NaN
                 if (__any_sync(0xffffffffu, need)) {
                     // O holds PV(j-1) already (S(j) was committed after it).
                     tmem_st_wait();
-                    const float m_new = need ? m_tile : m;
+                    const float m_tile = fmaxf(max64(s), max64(s + 64)) * sl2;
+                    const float m_new = need ? fmaxf(m_tile, m) : m;
                     const float alpha = ex2_approx(m - m_new);
                     l *= alpha;
 #pragma unroll

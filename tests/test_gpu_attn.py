@@ -89,6 +89,27 @@ def test_peaky_attention_large_outputs():
     parity.compare(O.double().cpu().numpy(), L.double().cpu().numpy(), Or, Lr, head_axes=(0, 2))
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_large_score_jumps_exercise_the_rescale_paths(D):
+    # Key tiles after the first hold scores far above its max: key 200 lifts P to
+    # about 2^23 (kept without a rescale), keys 450 and 600 push the row sum past
+    # 2^39 (the running max moves twice).  The oracle is exact for all of them.
+    B, N, H = 1, 640, 2
+    g = wl.generator(_dev(), 21)
+    q = torch.randn(B, N, H, D, generator=g, device=_dev()) * 0.1 + 0.5
+    k = torch.randn(B, N, H, D, generator=g, device=_dev()) * 0.1
+    v = torch.randn(B, N, H, D, generator=g, device=_dev())
+    scale = 8.0 / D        # 64-channel dot products of 0.5 * c land near 8c/D * 32 = 4c at D = 64
+    k[:, 200] += 4.0 * (64.0 / D)
+    k[:, 450] += 9.0 * (64.0 / D)
+    k[:, 600] += 20.0 * (64.0 / D)
+    q, k, v = (x.to(torch.bfloat16) for x in (q, k, v))
+    O, L = _attn(q, k, v, scale=scale)
+    torch.cuda.synchronize()
+    Or, Lr = parity.oracle_full(q, k, v, scale=scale)
+    parity.compare(O.double().cpu().numpy(), L.double().cpu().numpy(), Or, Lr, head_axes=(0, 2))
+
+
 def test_pad_keys_never_read_and_deterministic():
     B, N, H, D, kvl = 1, 700, 2, 128, 515
     q, k, v, _ = wl.make_qkv(B, N, H, D, seed=12, device=_dev())
