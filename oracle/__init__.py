@@ -12,6 +12,10 @@ Contents
 ``lse_merge``            batched (O, LSE) combine, fp64, numpy.
 ``lse_merge_streaming``  the same combine as a streaming pairwise recurrence.
 ``qkv_to_head_major``    the fused-QKV split/permute, numpy indexing.
+``e4m3_encode`` / ``e4m3_decode``  the FP8 E4M3 format (round to nearest even,
+                         saturating), numpy, from the format's definition.
+``qkv_cast_fp8``         the one-pass scaled cast of a stacked QKV buffer.
+``attn_fp8``             attention on E4M3 inputs with per-tensor descales.
 
 Citations (page title, section):
   * "Scaling Video Generation Across NVL72 rack with TensorRT-LLM":
@@ -30,6 +34,9 @@ Citations (page title, section):
     paragraph "构造 padding mask": key-only (1,1,T) mask, pads at the tail.
   * "CUDA IPC Ulysses：在 H100 上重叠 Attention 通信", "基线与瓶颈": V of a fused
     QKV projection is a legal strided view; no packing copy.
+  * NVL72 blog, "Ulysses Parallelism", paragraph on the stacked buffer: one
+    single-pass FP8 cast over the contiguous [B, S, 3, H, D] QKV buffer before
+    an FP8 attention kernel, whose result feeds the kernel without a copy.
 
 Parity status: every function here is pinned by the CPU tests (brute force,
 closed forms, library special cases and invariants); none is "parity unpinned".
@@ -210,3 +217,87 @@ def qkv_to_head_major(qkv: np.ndarray):
     if qkv.ndim != 5 or qkv.shape[2] != 3:
         raise ValueError("expected a [B, N, 3, H, D] array")
     return tuple(np.ascontiguousarray(qkv[:, :, t].transpose(0, 2, 1, 3)) for t in range(3))
+
+
+# ------------------------------------------------------------------ FP8 E4M3
+# E4M3 (the "fn" variant): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa
+# bits; no infinities; S.1111.111 is NaN; largest finite 448 = 1.75 * 2^8;
+# smallest normal 2^-6; subnormals m/8 * 2^-6, the smallest 2^-9.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """E4M3 bytes -> exact float64 values (NaN for S.1111.111)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, e - 7))
+    val = np.where((e == 0xF) & (m == 0x7), np.nan, val)
+    return sign * val
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """float64 -> E4M3 bytes: round to nearest, ties to even; magnitudes beyond
+    448 saturate to +-448; NaN -> 0x7F; the sign of zero is kept."""
+    x = np.asarray(x, dtype=np.float64)
+    neg = np.signbit(x)
+    a = np.abs(x)
+    out = np.zeros(a.shape, dtype=np.int64)
+    finite = np.isfinite(a)
+    # normal range: exponent from frexp (a = f * 2^k, f in [0.5, 1))
+    f, k = np.frexp(np.where(finite & (a > 0), a, 1.0))
+    e = k - 1                                    # a = (2f) * 2^e, 2f in [1, 2)
+    normal = finite & (a >= 2.0 ** -6)
+    mant = np.rint((2.0 * f - 1.0) * 8.0)        # ties to even
+    carry = mant >= 8
+    e = np.where(carry, e + 1, e)
+    mant = np.where(carry, 0, mant)
+    code_n = ((e + 7) << 3) + mant.astype(np.int64)
+    over = normal & ((e > 8) | ((e == 8) & (mant >= 7)))
+    code_n = np.where(over, 0x7E, code_n)
+    # subnormal range: multiples of 2^-9, ties to even (8 * 2^-9 is the smallest normal)
+    code_s = np.rint(np.where(finite, a, 0.0) / 2.0 ** -9).astype(np.int64)
+    out = np.where(normal, code_n, np.where(finite, code_s, 0x7E))
+    out = np.where(np.isnan(x), 0x7F, out)
+    out = np.where(neg, out | 0x80, out)
+    return out.astype(np.uint8)
+
+
+def qkv_cast_fp8(qkv_bits: np.ndarray, scales) -> np.ndarray:
+    """One-pass cast of a stacked [B, N, 3, H, D] bf16 buffer (uint16 bits) to
+    E4M3: out[b, n, t] = e4m3(x[b, n, t] * scales[t]) for t in (q, k, v)."""
+    x = bf16_bits_to_f64(qkv_bits)
+    sc = np.asarray(scales, dtype=np.float64).reshape(1, 1, 3, 1, 1)
+    # the scaled value is formed in fp32 on the device; it is exact in fp32
+    # whenever it is in range (bf16 * fp32 has at most 8 + 24 significant bits,
+    # rounded once), so form it in fp32 here too
+    y = (x.astype(np.float32) * sc.astype(np.float32)).astype(np.float64)
+    return e4m3_encode(y)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def e4m3_to_bf16_bits(codes: np.ndarray) -> np.ndarray:
+    """Every finite E4M3 value is exactly a bf16 value (3 <= 7 mantissa bits,
+    exponents 2^-9 .. 2^8); returns those bf16 bit patterns."""
+    v = e4m3_decode(codes).astype(np.float32)
+    return (v.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def attn_fp8(q8: np.ndarray, k8: np.ndarray, v8: np.ndarray, *, scale: float, descale_q: float,
+             descale_k: float, descale_v: float, key_valid_len: int | None = None,
+             rows: np.ndarray | None = None, threads: int = 0):
+    """Attention on E4M3 inputs q8, k8, v8 ([B, N, H, D] uint8 views) that stand
+    for Q = q8 * descale_q, K = k8 * descale_k, V = v8 * descale_v:
+    softmax(scale * Q K^T) V and its LSE, in fp64, through ``attn``."""
+    qb = e4m3_to_bf16_bits(q8)
+    kb = e4m3_to_bf16_bits(k8)
+    vb = e4m3_to_bf16_bits(v8)
+    O, L = attn(qb, kb, vb, key_valid_len=key_valid_len, scale=scale * descale_q * descale_k, rows=rows,
+                threads=threads)
+    return O * descale_v, L
