@@ -53,9 +53,9 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(main: str = "attn_fwd.cu") -> str:
     h = hashlib.sha256()
-    for fn in ("attn_fwd.cu", "ptx.cuh", "internal.h"):
+    for fn in (main, "ptx.cuh", "internal.h"):
         with open(os.path.join(ROOT, "dit_long_sequence_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -64,13 +64,14 @@ def kernel_source_hash() -> str:
 def profiled_traffic(workload: str):
     """dram bytes per attention launch from the committed ncu summary, if it was
     taken on the current kernel source; else None."""
-    p = os.path.join(ROOT, "profiles", f"attn_fwd_{workload}.md")
+    fp8 = workload.endswith("_fp8")
+    p = os.path.join(ROOT, "profiles", f"{'attn_fwd_fp8_' + workload[:-4] if fp8 else 'attn_fwd_' + workload}.md")
     if not os.path.exists(p):
         return None
     text = open(p, encoding="utf-8").read()
     m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash("attn_fwd_fp8.cu" if fp8 else "attn_fwd.cu"):
         return None
     return float(m_bytes.group(1))
 
@@ -192,8 +193,8 @@ class Step:
         self.stream = torch.cuda.current_stream(dev)
         B, N, H, D = w.B, w.N, w.H, w.D
         base = w.name.split("_h")[0]
-        self.mode = "layout+attn" if base in ("ltx2_padded", "tiny") else (
-            "chunked+merge" if w.kv_chunks > 1 else "attn")
+        self.mode = "cast+attn_fp8" if w.fp8 else ("layout+attn" if base in ("ltx2_padded", "tiny") else (
+            "chunked+merge" if w.kv_chunks > 1 else "attn"))
         if self.mode == "layout+attn" or w.fused:
             # one fused [B, N, 3, H, D] projection buffer is the step's input
             self.inputs = [wl.randn_bf16((B, N, 3, H, D), w.seed, dev)]
@@ -202,6 +203,9 @@ class Step:
             self.inputs = [q, k, v]
         if self.mode == "layout+attn":
             self.planes = tuple(torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev) for _ in range(3))
+        if self.mode == "cast+attn_fp8":
+            self.qkv8 = torch.empty((B, N, 3, H, D), dtype=torch.uint8, device=dev)
+            self.descales = tuple(1.0 / x for x in wl.FP8_SCALES)
         if self.mode == "chunked+merge":
             n = w.kv_chunks
             # per-row interleaved partials [B, N, H, n, D]: the merge reads one stream
@@ -210,13 +214,16 @@ class Step:
             self.l_parts = torch.empty((n, B, H, N), dtype=torch.float32, device=dev)
         self.out = torch.empty((B, N, H, D), dtype=torch.float32, device=dev)
         self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        self.launches_per_step = {"layout+attn": 2, "attn": 1, "chunked+merge": w.kv_chunks + 1}[self.mode]
+        self.launches_per_step = {"layout+attn": 2, "attn": 1, "chunked+merge": w.kv_chunks + 1,
+                                  "cast+attn_fp8": 2}[self.mode]
         self.attn_events = []
 
     def qkv_of(self, inputs):
         """The [B, N, H, D] q, k, v views the attention reads for these inputs."""
         if self.mode == "layout+attn":
             return tuple(p.permute(0, 2, 1, 3) for p in self.planes)
+        if self.mode == "cast+attn_fp8":
+            return self.qkv8[:, :, 0], self.qkv8[:, :, 1], self.qkv8[:, :, 2]
         if len(inputs) == 1:
             f = inputs[0]
             return f[:, :, 0], f[:, :, 1], f[:, :, 2]
@@ -240,6 +247,9 @@ class Step:
         dl, w = self.dl, self.w
         if self.mode == "layout+attn":
             dl.qkv_to_head_major(inputs[0], outs=self.planes, stream=stream)
+        if self.mode == "cast+attn_fp8":
+            from dit_long_sequence_gb300 import workloads as wl
+            dl.qkv_cast_fp8(inputs[0], wl.FP8_SCALES, out=self.qkv8, stream=stream)
         q, k, v = self.qkv_of(inputs)
         ev = None
         if record:
@@ -251,6 +261,8 @@ class Step:
             for c in range(n):
                 dl.attn_fwd(q, k[:, c * cl:(c + 1) * cl], v[:, c * cl:(c + 1) * cl],
                             out=self.o_parts[c], lse=self.l_parts[c], stream=stream)
+        elif self.mode == "cast+attn_fp8":
+            dl.attn_fwd_fp8(q, k, v, self.descales, key_valid_len=w.key_valid_len, out=out, lse=lse, stream=stream)
         else:
             dl.attn_fwd(q, k, v, key_valid_len=w.key_valid_len, out=out, lse=lse, stream=stream)
         if record:
@@ -305,19 +317,25 @@ def time_merge_kernel(dev, B, N, H, D, n_chunks=9, reps=5, interleaved=True):
 
 
 def time_layout_kernel(step, reps=5):
+    """HBM roofline of the step's layout kernel: the QKV split (2 + 2 bytes per
+    element) or the FP8 cast (2 + 1 bytes per element)."""
     import torch
-    if step.mode != "layout+attn":
+    from dit_long_sequence_gb300 import workloads as wl
+    if step.mode not in ("layout+attn", "cast+attn_fp8"):
         return None
     s = step.stream
     ts = []
     for _ in range(reps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(s)
-        step.dl.qkv_to_head_major(step.inputs[0], outs=step.planes, stream=s)
+        if step.mode == "layout+attn":
+            step.dl.qkv_to_head_major(step.inputs[0], outs=step.planes, stream=s)
+        else:
+            step.dl.qkv_cast_fp8(step.inputs[0], wl.FP8_SCALES, out=step.qkv8, stream=s)
         b.record(s)
         b.synchronize()
         ts.append(a.elapsed_time(b))
-    nbytes = 2 * step.inputs[0].numel() * 2
+    nbytes = step.inputs[0].numel() * (4 if step.mode == "layout+attn" else 3)
     return nbytes, statistics.median(ts)
 
 
@@ -325,15 +343,20 @@ def time_layout_kernel(step, reps=5):
 
 def cpu_baseline(w, dev_inputs=None, target_s=12.0):
     """The fp64 oracle as it stands, on a bounded sample of query rows of the
-    workload (all keys), on the host cores.  Returns a dict in the metric's unit."""
+    workload (all keys), on the host cores.  Returns a dict in the metric's unit.
+    FP8 workloads: dev_inputs are the E4M3 code views and the oracle's FP8
+    attention runs on them."""
     import numpy as np
     import oracle
     from dit_long_sequence_gb300 import workloads as wl
     if dev_inputs is None:
-        q, k, v, _ = wl.make_workload_inputs(w, device="cpu")
+        dev_inputs = baseline_inputs(w)
+    q, k, v = dev_inputs
+    if w.fp8:
+        qb, kb, vb = (u8_host(t) for t in (q, k, v))
+        d = tuple(1.0 / x for x in wl.FP8_SCALES)
     else:
-        q, k, v = dev_inputs
-    qb, kb, vb = wl.host_bf16_bits(q), wl.host_bf16_bits(k), wl.host_bf16_bits(v)
+        qb, kb, vb = wl.host_bf16_bits(q), wl.host_bf16_bits(k), wl.host_bf16_bits(v)
     kvl = w.key_valid_len
     per_row = 4.0 * w.kv_len * w.D
 
@@ -341,7 +364,11 @@ def cpu_baseline(w, dev_inputs=None, target_s=12.0):
         rows = wl.sample_rows(1, heads, w.N, rows_per_head, seed=w.seed)
         qs, ks, vs = qb[:1, :, :heads], kb[:1, :, :heads], vb[:1, :, :heads]
         t0 = time.perf_counter()
-        oracle.attn(qs, ks, vs, key_valid_len=kvl, rows=rows)
+        if w.fp8:
+            oracle.attn_fp8(qs, ks, vs, scale=w.scale, descale_q=d[0], descale_k=d[1], descale_v=d[2],
+                            key_valid_len=kvl, rows=rows)
+        else:
+            oracle.attn(qs, ks, vs, key_valid_len=kvl, rows=rows)
         return time.perf_counter() - t0, rows.size
 
     heads = min(w.H, 8)
@@ -362,14 +389,37 @@ def cpu_baseline(w, dev_inputs=None, target_s=12.0):
             "extrapolated_full_step_s": (w.flops() / per_row) / (n / t)}
 
 
+def baseline_inputs(w, heads=8):
+    """Host inputs of the CPU baseline: the workload's bf16 q, k, v; for FP8
+    workloads the oracle's E4M3 cast of batch 0, heads < `heads` of the same
+    seeded stacked buffer (all the sample reads)."""
+    import torch
+    import oracle
+    from dit_long_sequence_gb300 import workloads as wl
+    if not w.fp8:
+        return wl.make_workload_inputs(w, device="cpu")[:3]
+    buf = wl.randn_bf16((w.B, w.N, 3, w.H, w.D), w.seed, "cpu")[:1, :, :, :heads]
+    codes = oracle.qkv_cast_fp8(wl.host_bf16_bits(buf.contiguous()), wl.FP8_SCALES)
+    return tuple(torch.from_numpy(codes[:, :, t]) for t in range(3))
+
+
+def u8_host(t):
+    """Host numpy copy of a (possibly strided) uint8 view, strides kept."""
+    import torch
+    if t.device.type == "cpu":
+        return t.numpy()
+    n = t.untyped_storage().nbytes()
+    base = torch.empty(0, dtype=torch.uint8, device=t.device).set_(t.untyped_storage(), 0, (n,), (1,))
+    return base.cpu().as_strided(t.shape, t.stride(), t.storage_offset()).numpy()
+
+
 # ------------------------------------------------------------------------ main
 
 def run_reference(args, w):
     rank, world, _ = dist_setup(args.gpus)
     if rank != 0:
         return 0
-    from dit_long_sequence_gb300 import workloads as wl
-    q, k, v, _ = wl.make_workload_inputs(w, device="cpu")
+    q, k, v = baseline_inputs(w)
     for _ in range(args.warmup):
         cpu_baseline(w, (q, k, v), target_s=1.0)
     if args.steps is None:
@@ -380,7 +430,7 @@ def run_reference(args, w):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(args.steps, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded bf16 N(0,1))",
+            "data": "synthetic (seeded bf16 N(0,1)" + (", cast to E4M3 by the oracle)" if w.fp8 else ")"),
             "config": config_of(w),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": vals[-1]["cores"], "kind": "oracle",
                              "sample": vals[-1]["sample"] + " per step"},
@@ -392,6 +442,7 @@ def run_reference(args, w):
 def config_of(w):
     return {"workload": w.name, "B": w.B, "H": w.H, "D": w.D, "seq_len": w.N,
             "key_valid_len": w.kv_len, "kv_chunks": w.kv_chunks, "fused_qkv": w.fused,
+            "inputs": "e4m3 (one-pass cast of the stacked bf16 buffer, scales 64)" if w.fp8 else "bf16",
             "out_dtype": "fp32", "global_batch": w.B, "l2": "inputs larger than the 129 MB L2, no flush",
             "description": w.description}
 
@@ -459,12 +510,16 @@ def main(argv=None):
     attn_ms = step.attn_ms_per_launch()
     per_launch_flops = flops_step / (w.kv_chunks if w.kv_chunks > 1 else 1)
     peaks, peak_kind = load_peaks()
-    peak = float(peaks["bf16_tflops"])
+    bf16_peak = float(peaks["bf16_tflops"])
+    # FP8 contraction: the measured bf16 peak x the nominal fp8 / bf16 ratio (4.5 / 2.25)
+    peak = 2.0 * bf16_peak if w.fp8 else bf16_peak
     achieved = per_launch_flops / (attn_ms * 1e-3) / 1e12
     traffic = profiled_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": "attn_fwd_kernel<128,false>", "peak_kind": f"{peak_kind} dense bf16 burst",
+                "kernel": "attn_fwd_fp8_kernel<false>" if w.fp8 else "attn_fwd_kernel<128,false,false>",
+                "peak_kind": (f"{peak_kind} dense bf16 burst x 2 (nominal fp8/bf16 ratio)" if w.fp8
+                              else f"{peak_kind} dense bf16 burst"),
                 "flops_per_launch": per_launch_flops, "ms_per_launch": attn_ms}
 
     # ---------------- secondary HBM-bound kernels
@@ -472,7 +527,7 @@ def main(argv=None):
     lay = time_layout_kernel(step)
     if lay is not None:
         gbs = lay[0] / (lay[1] * 1e-3) / 1e9
-        extra["layout"] = {"bytes": lay[0], "ms": lay[1], "GB/s": gbs, "frac_hbm": gbs / float(peaks["hbm_gbs"])}
+        extra["cast_fp8" if w.fp8 else "layout"] = {"bytes": lay[0], "ms": lay[1], "GB/s": gbs, "frac_hbm": gbs / float(peaks["hbm_gbs"])}
     for il, key in ((True, "merge_n9_interleaved"), (False, "merge_n9_chunk_major")):
         mb, mms = time_merge_kernel(dev, w.B, w.N, w.H, w.D, n_chunks=9, interleaved=il)
         mgbs = mb / (mms * 1e-3) / 1e9
@@ -485,10 +540,11 @@ def main(argv=None):
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded bf16 N(0,1), no weights)",
+            "vs_baseline": None, "dtype": "e4m3" if w.fp8 else "bf16",
+            "data": "synthetic (seeded bf16 N(0,1), no weights)",
             "config": config_of(w), "roofline": roofline, "clocks": clk.summary(),
             "gpu_launches": step.launches_per_step * args.steps, "e2e": e2e, "kernels": extra,
-            "pct_of_bf16_peak": 100.0 * value / world / peak}
+            "pct_of_bf16_peak": 100.0 * value / world / bf16_peak}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, (step.q, step.k, step.v))
     if rank == 0:

@@ -44,6 +44,11 @@ _lib.dit_attn_fwd.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i
 _lib.dit_attn_fwd_accumulate.restype = _i
 _lib.dit_attn_fwd_accumulate.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
                                          _vp, _vp, _vp]
+_lib.dit_attn_fwd_fp8.restype = _i
+_lib.dit_attn_fwd_fp8.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f, _f, _f, _f,
+                                  _vp, _i, _vp, _vp]
+_lib.dit_qkv_cast_fp8.restype = _i
+_lib.dit_qkv_cast_fp8.argtypes = [_vp, _i64, _i64, _i, _i, _i, _i, _f, _f, _f, _vp, _vp]
 _lib.dit_watchdog_selftest.restype = _i
 _lib.dit_watchdog_selftest.argtypes = [ctypes.c_uint32, _vp]
 _lib.dit_attn_lse_merge.restype = _i
@@ -57,7 +62,8 @@ _lib.dit_check_watchdog.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
 _lib.dit_version.restype = ctypes.c_uint32
 
 EXPORTS = ("dit_attn_fwd", "dit_attn_fwd_accumulate", "dit_attn_lse_merge", "dit_qkv_to_head_major",
-           "dit_status_string", "dit_check_watchdog", "dit_watchdog_selftest", "dit_version")
+           "dit_qkv_cast_fp8", "dit_attn_fwd_fp8", "dit_status_string", "dit_check_watchdog",
+           "dit_watchdog_selftest", "dit_version")
 
 
 class DitError(RuntimeError):
@@ -195,6 +201,67 @@ def qkv_to_head_major(qkv: torch.Tensor, *, outs=None, stream=None):
                                     _stream_ptr(stream))
     _check(rc, "dit_qkv_to_head_major")
     return outs
+
+
+_FP8_DTYPES = (torch.uint8, torch.float8_e4m3fn)
+
+
+def qkv_cast_fp8(qkv: torch.Tensor, scales, *, out: torch.Tensor | None = None, stream=None):
+    """One-pass E4M3 cast of a stacked [B, N, 3, H, D] bf16 buffer (b and n
+    strides free, inner [3, H, D] contiguous), q/k/v scaled by scales[0..2],
+    through `dit_qkv_cast_fp8`.  Returns the contiguous [B, N, 3, H, D] result
+    (uint8 codes unless `out` is given as float8_e4m3fn)."""
+    B, N, three, H, D = qkv.shape
+    if three != 3 or qkv.dtype != torch.bfloat16 or not qkv.is_cuda:
+        raise ValueError("expected a bf16 CUDA [B, N, 3, H, D] tensor")
+    if qkv.stride(4) != 1 or qkv.stride(3) != D or qkv.stride(2) != H * D:
+        raise ValueError("the [3, H, D] block of every sequence row must be contiguous")
+    sq, sk, sv = (float(x) for x in scales)
+    if out is None:
+        out = torch.empty((B, N, 3, H, D), dtype=torch.uint8, device=qkv.device)
+    if out.dtype not in _FP8_DTYPES or tuple(out.shape) != (B, N, 3, H, D) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous uint8 / float8_e4m3fn [B, N, 3, H, D] tensor")
+    rc = _lib.dit_qkv_cast_fp8(qkv.data_ptr(), qkv.stride(0), qkv.stride(1), B, N, H, D, sq, sk, sv,
+                               out.data_ptr(), _stream_ptr(stream))
+    _check(rc, "dit_qkv_cast_fp8")
+    return out
+
+
+def attn_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, descales, *, key_valid_len: int | None = None,
+                 scale: float | None = None, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                 out_dtype: torch.dtype = torch.float32, stream=None):
+    """Attention on E4M3 codes through `dit_attn_fwd_fp8`: q, k, v [B, N, H, D]
+    uint8 / float8_e4m3fn views (e.g. of qkv_cast_fp8's output) standing for
+    q * descales[0], k * descales[1], v * descales[2].  Returns (out, lse)."""
+    B, Nq, H, D = q.shape
+    Nkv = k.shape[1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype not in _FP8_DTYPES or not t.is_cuda:
+            raise TypeError(f"{name} must be a uint8 / float8_e4m3fn CUDA tensor")
+    if k.shape != (B, Nkv, H, D) or v.shape != (B, Nkv, H, D):
+        raise ValueError("k and v must be [B, Nkv, H, D] matching q")
+    dq, dk, dv = (float(x) for x in descales)
+    kvl = Nkv if key_valid_len is None else int(key_valid_len)
+    sc = float(D) ** -0.5 if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, Nq, H, D), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if out.dtype not in (torch.float32, torch.bfloat16) or tuple(out.shape) != (B, Nq, H, D):
+        raise ValueError("out must be a [B, Nq, H, D] fp32 or bf16 tensor")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
+    st = AttnStrides(_strides4(q), _strides4(k), _strides4(v), _strides4(out))
+    rc = _lib.dit_attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(st), B, Nq, Nkv, H, D, kvl,
+                               sc, dq, dk, dv, out.data_ptr(), DIT_F32 if out.dtype == torch.float32 else DIT_BF16,
+                               lse.data_ptr(), _stream_ptr(stream))
+    _check(rc, "dit_attn_fwd_fp8")
+    return out, lse
+
+
+def split_stacked_fp8(qkv8: torch.Tensor):
+    """The q, k, v [B, N, H, D] views of a stacked [B, N, 3, H, D] FP8 buffer."""
+    return qkv8[:, :, 0], qkv8[:, :, 1], qkv8[:, :, 2]
 
 
 def watchdog_selftest(limit_us: int = 100_000, stream=None):

@@ -63,31 +63,33 @@ unsigned int* status_word(int dev) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// A [B, N, H, D] bf16 view as a 4-D TMA map (D, N, H, B), box (64, 128, 1, 1),
-// 128-byte swizzle.  Rows n >= n_rows are outside the map and read as zeros.
+// A [B, N, H, D] view as a 4-D TMA map (D, N, H, B) with 128-byte swizzle and
+// a box of one swizzle column (64 bf16 or 128 E4M3 channels) by 128 rows.
+// Rows n >= n_rows are outside the map and read as zeros.
 dit_status_t encode_view(CUtensorMap* map, const void* base, const dit_strides4_t& s, int B, int n_rows, int H,
-                         int D) {
+                         int D, bool fp8 = false) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return DIT_ERR_CUDA;
+    const cuuint64_t eb = fp8 ? 1 : 2;
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(n_rows > 0 ? n_rows : 1),
                                 static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
-    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.n) * 2, static_cast<cuuint64_t>(s.h) * 2,
-                                   static_cast<cuuint64_t>(s.b) * 2};
-    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(s.n) * eb, static_cast<cuuint64_t>(s.h) * eb,
+                                   static_cast<cuuint64_t>(s.b) * eb};
+    const cuuint32_t box[4] = {fp8 ? 128u : 64u, 128, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DIT_OK : DIT_ERR_INVALID_ARG;
 }
 
-// b, n, h strides of a bf16 TMA operand: positive, 16-byte multiples, < 2^39 elements.
-dit_status_t check_tma_strides(const dit_strides4_t& s) {
+// b, n, h strides of a TMA operand: positive, 16-byte multiples, < 2^39 elements.
+dit_status_t check_tma_strides(const dit_strides4_t& s, bool fp8 = false) {
     if (s.d != 1) return DIT_ERR_UNSUPPORTED;
     const int64_t st[3] = {s.b, s.n, s.h};
     for (int64_t x : st) {
         if (x <= 0 || x >= (int64_t(1) << 39)) return DIT_ERR_INVALID_ARG;
-        if (x % 8 != 0) return DIT_ERR_ALIGNMENT;
+        if (x % (fp8 ? 16 : 8) != 0) return DIT_ERR_ALIGNMENT;
     }
     return DIT_OK;
 }
@@ -115,14 +117,25 @@ extern "C" {
 
 namespace {
 
+// fp8: E4M3 inputs (D = 128 only), descales[3] = (q, k, v); otherwise bf16.
 dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides, int B,
                              int Nq, int Nkv, int H, int D, int key_valid_len, float scale, void* out,
-                             dit_dtype_t out_dtype, float* lse, bool accumulate, dit_stream_t stream) {
+                             dit_dtype_t out_dtype, float* lse, bool accumulate, dit_stream_t stream,
+                             const float* descales = nullptr) {
+    const bool fp8 = descales != nullptr;
     if (strides == nullptr) return DIT_ERR_INVALID_ARG;
     if (B < 0 || Nq < 0 || Nkv < 0 || H < 0) return DIT_ERR_INVALID_ARG;
     if (key_valid_len < 0 || key_valid_len > Nkv) return DIT_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return DIT_ERR_INVALID_ARG;
     if (out_dtype != DIT_BF16 && out_dtype != DIT_F32) return DIT_ERR_INVALID_ARG;
+    double sl2 = static_cast<double>(scale) * 1.4426950408889634;
+    if (fp8) {
+        for (int i = 0; i < 3; ++i)
+            if (!(descales[i] > 0.f) || !std::isfinite(descales[i])) return DIT_ERR_INVALID_ARG;
+        sl2 *= static_cast<double>(descales[0]) * static_cast<double>(descales[1]);
+        if (!(sl2 > 1e-30 && sl2 < 1e30)) return DIT_ERR_INVALID_ARG;
+        if (D != 128) return DIT_ERR_UNSUPPORTED;
+    }
     if (D != 64 && D != 128) return DIT_ERR_UNSUPPORTED;
     if (B > 65535 || H > 65535) return DIT_ERR_UNSUPPORTED;
     if (B == 0 || Nq == 0 || H == 0) return DIT_OK;
@@ -144,13 +157,13 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
     std::memset(&tv, 0, sizeof tv);
     if (any_keys) {
         dit_status_t st;
-        if ((st = check_tma_strides(strides->q)) != DIT_OK) return st;
-        if ((st = check_tma_strides(strides->k)) != DIT_OK) return st;
-        if ((st = check_tma_strides(strides->v)) != DIT_OK) return st;
+        if ((st = check_tma_strides(strides->q, fp8)) != DIT_OK) return st;
+        if ((st = check_tma_strides(strides->k, fp8)) != DIT_OK) return st;
+        if ((st = check_tma_strides(strides->v, fp8)) != DIT_OK) return st;
         if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return DIT_ERR_ALIGNMENT;
-        if ((st = encode_view(&tq, q, strides->q, B, Nq, H, D)) != DIT_OK) return st;
-        if ((st = encode_view(&tk, k, strides->k, B, key_valid_len, H, D)) != DIT_OK) return st;
-        if ((st = encode_view(&tv, v, strides->v, B, key_valid_len, H, D)) != DIT_OK) return st;
+        if ((st = encode_view(&tq, q, strides->q, B, Nq, H, D, fp8)) != DIT_OK) return st;
+        if ((st = encode_view(&tk, k, strides->k, B, key_valid_len, H, D, fp8)) != DIT_OK) return st;
+        if ((st = encode_view(&tv, v, strides->v, B, key_valid_len, H, D, fp8)) != DIT_OK) return st;
     }
 
     int dev = 0;
@@ -160,7 +173,8 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
     a.H = H;
     a.kv_len = key_valid_len;
     a.n_kv_tiles = (key_valid_len + 127) / 128;
-    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    a.scale_log2 = static_cast<float>(sl2);
+    a.o_scale = fp8 ? descales[2] : 1.f;
     a.out = out;
     a.o_sb = so.b;
     a.o_sn = so.n;
@@ -169,8 +183,10 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
     a.status = status_word(dev);
     a.timeout_ns = kWatchdogNs;
     if (a.status == nullptr) return DIT_ERR_CUDA;
-    cudaError_t e = launch_attn_fwd(tq, tk, tv, a, B, D, out_dtype == DIT_BF16, accumulate,
-                                    reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = fp8 ? launch_attn_fwd_fp8(tq, tk, tv, a, B, out_dtype == DIT_BF16,
+                                              reinterpret_cast<cudaStream_t>(stream))
+                        : launch_attn_fwd(tq, tk, tv, a, B, D, out_dtype == DIT_BF16, accumulate,
+                                          reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DIT_OK : DIT_ERR_CUDA;
 }
 
@@ -190,6 +206,45 @@ dit_status_t dit_attn_fwd_accumulate(const void* q, const void* k, const void* v
                                      float* lse, dit_stream_t stream) {
     return attn_fwd_common(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, scale, out, DIT_F32, lse, true,
                            stream);
+}
+
+dit_status_t dit_attn_fwd_fp8(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides,
+                              int B, int Nq, int Nkv, int H, int D, int key_valid_len, float scale, float descale_q,
+                              float descale_k, float descale_v, void* out, dit_dtype_t out_dtype, float* lse,
+                              dit_stream_t stream) {
+    const float descales[3] = {descale_q, descale_k, descale_v};
+    return attn_fwd_common(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, scale, out, out_dtype, lse, false,
+                           stream, descales);
+}
+
+dit_status_t dit_qkv_cast_fp8(const void* qkv, int64_t stride_b, int64_t stride_n, int B, int N, int H, int D,
+                              float scale_q, float scale_k, float scale_v, void* out, dit_stream_t stream) {
+    if (B < 0 || N < 0 || H < 0 || D < 0) return DIT_ERR_INVALID_ARG;
+    const float sc[3] = {scale_q, scale_k, scale_v};
+    for (float x : sc)
+        if (!(x > 0.f) || !std::isfinite(x)) return DIT_ERR_INVALID_ARG;
+    if (D % 16 != 0) return DIT_ERR_UNSUPPORTED;
+    if (B == 0 || N == 0 || H == 0 || D == 0) return DIT_OK;
+    if (qkv == nullptr || out == nullptr) return DIT_ERR_INVALID_ARG;
+    const uint64_t hd = static_cast<uint64_t>(H) * static_cast<uint64_t>(D);
+    const uint64_t chunks = 3 * hd / 16;
+    if (3 * hd > (uint64_t(1) << 28) || static_cast<uint64_t>(B) * N * chunks >= (uint64_t(1) << 32))
+        return DIT_ERR_UNSUPPORTED;
+    if (stride_b < 0 || stride_n < 0) return DIT_ERR_INVALID_ARG;
+    if (stride_b % 8 || stride_n % 8) return DIT_ERR_ALIGNMENT;
+    if (!aligned16(qkv) || !aligned16(out)) return DIT_ERR_ALIGNMENT;
+    CastArgs a;
+    a.qkv = static_cast<const uint16_t*>(qkv);
+    a.stride_b = stride_b;
+    a.stride_n = stride_n;
+    a.N = N;
+    a.hd = static_cast<uint32_t>(hd);
+    a.chunks_per_row = static_cast<uint32_t>(chunks);
+    a.total_chunks = static_cast<uint64_t>(B) * N * chunks;
+    for (int i = 0; i < 3; ++i) a.scale[i] = sc[i];
+    a.out = static_cast<uint8_t*>(out);
+    cudaError_t e = launch_qkv_cast_fp8(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DIT_OK : DIT_ERR_CUDA;
 }
 
 dit_status_t dit_attn_lse_merge(const float* o_parts, int64_t o_chunk_stride, int64_t o_row_stride,

@@ -1,0 +1,391 @@
+// attn_fwd_fp8.cu -- attention forward on E4M3 Q/K/V (head dim 128), sm_103a,
+// TMA + tcgen05 kind::f8f6f4, fp32 accumulators in TMEM.
+//
+// The FP8 attention that "Scaling Video Generation Across NVL72 rack with
+// TensorRT-LLM" ("Ulysses Parallelism", paragraph "Fused vs. unfused QKV
+// all-to-all") feeds with the one-pass cast of the stacked QKV buffer: the
+// cast output is read in place through (b, n, h) strides.  Q, K, V stand for
+// q8 * descale_q, k8 * descale_k, v8 * descale_v; the kernel computes
+//     O = softmax(scale * Q K^T) V,   LSE = ln sum_j exp(scale * q . k_j)
+// exactly as the bf16 kernel does, with S = q8 . k8 accumulated in fp32 and
+// scale * descale_q * descale_k folded into the exponent.
+//
+// Same CTA shape, warp roles, TMEM map and product order as the bf16 kernel
+// (256 query rows of one head as two 128-row tiles; warps 0-7 softmax, warp 8
+// MMA, warp 9 TMA).  A 128 x 128 E4M3 tile is 16 KB and exactly one 128-byte
+// swizzle column wide, so every tile moves in one TMA copy and the ring holds
+// eight stages.  Each product is four K = 32 instructions.
+//
+// P is fed to the PV product as E4M3 (four keys per 32-bit TMEM column, the
+// lowest key in the lowest byte), so it must stay <= 448.  P = 2^(x - m + 7),
+// x = s * scale * log2(e), with m the running row max; m moves only when a
+// tile's max exceeds it by more than 1.75, so P <= 2^8.75 < 448, and the
+// smallest kept values (2^-9) are ~2^-16 below the row max.  Unlike the bf16
+// kernel, this needs the tile max every tile.  The row sum l accumulates the
+// unrounded fp32 P; O = (sum P v8) * descale_v / l.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dit {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kD = 128;
+constexpr int kThreads = 384;
+constexpr uint32_t kSoftmaxRegs = 208;
+constexpr uint32_t kOtherRegs = 88;
+static_assert(256 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * 168, "register split");
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kPOffset = 7.f;   // P = 2^(x - m + kPOffset)
+constexpr float kStale = 1.75f;   // keep m while the tile max is <= m + kStale
+
+constexpr int kTile = kBM * kD;   // bytes of one 128 x 128 E4M3 tile
+constexpr int kStages = 8;
+constexpr int kQFull = 0;
+constexpr int kKVFull = 2;
+constexpr int kKVEmpty = kKVFull + kStages;
+constexpr int kSFull = kKVEmpty + kStages;
+constexpr int kPFull = kSFull + 2;
+constexpr int kOFinal = kPFull + 2;
+constexpr int kDrain = kOFinal + 2;
+constexpr int kLoadDrain = kDrain + 1;
+constexpr int kNumBars = kLoadDrain + 1;
+constexpr int kBarOffset = (2 + kStages) * kTile;
+constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+static_assert(kSmemBytes <= 232448, "shared memory");
+
+__device__ __forceinline__ float max64(const float* v) {
+    float t8[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t8[k] = max3f(v[k], v[8 + k], v[16 + k]);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t8[k] = max3f(t8[k], v[24 + k], v[32 + k]);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t8[k] = max3f(t8[k], v[40 + k], v[48 + k]);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t8[k] = fmaxf(t8[k], v[56 + k]);
+    return max3f(max3f(t8[0], t8[1], t8[2]), max3f(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
+}
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
+    constexpr int S = kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t sQ = s_base;                  // Q tile t at sQ + t*kTile
+    const uint32_t sRing = s_base + 2 * kTile;   // slot s at sRing + s*kTile
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffset);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* never_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+    auto bar = [&](int i) -> uint32_t { return smem_u32(bars + i); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int h = blockIdx.y;
+    const int b = blockIdx.z;
+    const int q_row0 = blockIdx.x * (2 * kBM);
+    const int n_tiles = a.n_kv_tiles;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(kQFull + 0), 1);
+        mbar_init(bar(kQFull + 1), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar(kKVFull + s), 1);
+            mbar_init(bar(kKVEmpty + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(kSFull + t), 1);
+            mbar_init(bar(kPFull + t), 128);
+            mbar_init(bar(kOFinal + t), 1);
+        }
+        mbar_init(bar(kDrain), 1);
+        mbar_init(bar(kLoadDrain), 1);
+        *abort_flag = 0;
+        *never_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 8) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Watchdog wd{a.status, a.timeout_ns, abort_flag};
+    const Watchdog wd_drain{a.status, a.timeout_ns, never_flag};
+
+    if (warp >= 10) {
+        regs_decrease<kOtherRegs>();
+    } else if (warp == 9) {
+        regs_decrease<kOtherRegs>();
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && n_tiles > 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            for (int t = 0; t < 2; ++t) {
+                mbar_arrive_expect_tx(bar(kQFull + t), kTile);
+                tma_load_4d(sQ + t * kTile, &tm_q, bar(kQFull + t), 0, q_row0 + t * kBM, h, b);
+            }
+            const int total = 2 * n_tiles;
+            int issued = 0;
+            for (int i = 0; i < total; ++i) {
+                const int slot = i % S;
+                const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
+                if (!wait_bounded(bar(kKVEmpty + slot), ph ^ 1u, wd, ROLE_LOAD, SITE_KV_EMPTY)) break;
+                mbar_arrive_expect_tx(bar(kKVFull + slot), kTile);
+                tma_load_4d(sRing + slot * kTile, (i & 1) ? &tm_v : &tm_k, bar(kKVFull + slot), 0, (i >> 1) * kBN, h,
+                            b);
+                issued = i + 1;
+            }
+            if (issued < total || *abort_flag) {
+                for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
+                    wait_bounded(bar(kKVFull + i % S), static_cast<uint32_t>(i / S) & 1u, wd_drain, ROLE_LOAD,
+                                 SITE_LOAD_DRAIN);
+                wait_bounded(bar(kQFull + 0), 0, wd_drain, ROLE_LOAD, SITE_LOAD_DRAIN);
+                wait_bounded(bar(kQFull + 1), 0, wd_drain, ROLE_LOAD, SITE_LOAD_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 8) {
+        regs_decrease<kOtherRegs>();
+        // ------------------------------------------------------------- MMA issuer
+        if (lane == 0 && n_tiles > 0) {
+            constexpr uint32_t kIdescQK = idesc_e4m3_f32(kBM, kBN, false);
+            constexpr uint32_t kIdescPV = idesc_e4m3_f32(kBM, kD, true);
+            const uint32_t tS0 = tmem, tS1 = tmem + 128;
+            const uint32_t tO0 = tmem + 256, tO1 = tmem + 256 + kD;
+
+            // S_t = Q_t K^T: both K-major, 32 channels (32 bytes) per instruction.
+            auto issue_qk = [&](uint32_t tS, uint32_t q_addr, uint32_t k_addr) {
+#pragma unroll
+                for (int kk = 0; kk < kD / 32; ++kk)
+                    umma_ss_f8(tS, sdesc_sw128(q_addr + kk * 32, 16, 1024), sdesc_sw128(k_addr + kk * 32, 16, 1024),
+                               kIdescQK, kk > 0 ? 1u : 0u);
+            };
+            // O_t (+)= P_t V: P from TMEM (8 columns = 32 keys per instruction),
+            // V MN-major, 32 keys = four 8-row swizzle atoms = 4096 bytes.
+            auto issue_pv = [&](uint32_t tO, uint32_t tP, uint32_t v_addr, bool accumulate) {
+#pragma unroll
+                for (int kk = 0; kk < kBN / 32; ++kk)
+                    umma_ts_f8(tO, tP + kk * 8, sdesc_sw128(v_addr + kk * 4096, 16384, 1024), kIdescPV,
+                               (accumulate || kk > 0) ? 1u : 0u);
+            };
+
+            bool ok = wait_bounded(bar(kQFull + 0), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
+                      wait_bounded(bar(kQFull + 1), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
+                      wait_bounded(bar(kKVFull + 0), 0, wd, ROLE_MMA, SITE_KV_FULL);
+            if (ok) {
+                tc_fence_after();
+                issue_qk(tS0, sQ, sRing);
+                umma_commit(bar(kSFull + 0));
+                issue_qk(tS1, sQ + kTile, sRing);
+                umma_commit(bar(kSFull + 1));
+                umma_commit(bar(kKVEmpty + 0));
+            }
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int iv = 2 * j + 1, ik = 2 * j + 2;
+                const uint32_t v_addr = sRing + (iv % S) * kTile;
+                const uint32_t k_addr = sRing + (ik % S) * kTile;
+                const bool more = j + 1 < n_tiles;
+                const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+                ok = wait_bounded(bar(kKVFull + iv % S), static_cast<uint32_t>(iv / S) & 1u, wd, ROLE_MMA,
+                                  SITE_KV_FULL) &&
+                     wait_bounded(bar(kPFull + 0), ph, wd, ROLE_MMA, SITE_P_FULL);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(tO0, tS0, v_addr, j > 0);
+                if (more) {
+                    ok = wait_bounded(bar(kKVFull + ik % S), static_cast<uint32_t>(ik / S) & 1u, wd, ROLE_MMA,
+                                      SITE_KV_FULL);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_qk(tS0, sQ, k_addr);
+                    umma_commit(bar(kSFull + 0));
+                } else {
+                    umma_commit(bar(kOFinal + 0));
+                }
+                ok = wait_bounded(bar(kPFull + 1), ph, wd, ROLE_MMA, SITE_P_FULL);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(tO1, tS1, v_addr, j > 0);
+                umma_commit(bar(kKVEmpty + iv % S));
+                if (more) {
+                    issue_qk(tS1, sQ + kTile, k_addr);
+                    umma_commit(bar(kSFull + 1));
+                    umma_commit(bar(kKVEmpty + ik % S));
+                } else {
+                    umma_commit(bar(kOFinal + 1));
+                }
+            }
+            umma_commit(bar(kDrain));
+            wait_bounded(bar(kDrain), 0, wd_drain, ROLE_MMA, SITE_DRAIN);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------- softmax warps
+        regs_increase<kSoftmaxRegs>();
+        const int t = warp >> 2;
+        const int wq = warp & 3;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + t * 128;
+        const uint32_t tO = tmem + lane_off + 256 + t * kD;
+        const int row = q_row0 + t * kBM + wq * 32 + lane;
+        const float sl2 = a.scale_log2;
+        float m = -INFINITY;  // running max of x = s * sl2 (possibly stale by <= kStale)
+        float l = 0.f;        // running sum of 2^(x - m + kPOffset)
+        bool ok = true;
+
+        // P for 64 scores -> 16 TMEM columns of four E4M3 at tP; returns sum P.
+        auto exp_store = [&](const float* v, uint32_t tP, float neg) {
+            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float x0, x1, x2, x3;
+                ffma2_bc(x0, x1, v[4 * i], v[4 * i + 1], sl2, neg);
+                ffma2_bc(x2, x3, v[4 * i + 2], v[4 * i + 3], sl2, neg);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+                fadd2_acc(a0, a1, p0, p1);
+                fadd2_acc(b0, b1, p2, p3);
+                pk[i] = pack_e4m3x4(p0, p1, p2, p3);
+            }
+            tmem_st16(tP, pk);
+            return (a0 + a1) + (b0 + b1);
+        };
+
+        for (int j = 0; j < n_tiles; ++j) {
+            ok = wait_bounded(bar(kSFull + t), static_cast<uint32_t>(j) & 1u, wd, ROLE_SOFTMAX, SITE_S_FULL);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+
+            uint32_t sr[4][32];
+            tmem_ld32(tS + 0, sr[0]);
+            tmem_ld32(tS + 32, sr[1]);
+            tmem_ld32(tS + 64, sr[2]);
+            tmem_ld32(tS + 96, sr[3]);
+            tmem_ld_wait_dep(sr[0]);
+            reg_dep(sr[1]);
+            reg_dep(sr[2]);
+            reg_dep(sr[3]);
+            const int valid = a.kv_len - j * kBN;   // >= 1
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+            if (valid < 128) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c >= valid) s[c] = -INFINITY;
+            }
+            const float mx = fmaxf(max64(s), max64(s + 64)) * sl2;
+            const bool need = mx > m + kStale;   // always true on the first tile
+            if (__any_sync(0xffffffffu, need)) {
+                const float m_new = need ? mx : m;
+                const float alpha = ex2_approx(m - m_new);
+                l *= alpha;
+                if (j > 0) {
+                    // O holds PV(j-1): S(j) was committed after it.
+#pragma unroll
+                    for (int cc = 0; cc < kD / 32; ++cc) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + cc * 32, o);
+                        tmem_ld_wait_dep(o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tO + cc * 32, o);
+                    }
+                }
+                m = m_new;
+            }
+            const float neg = kPOffset - m;
+            l += exp_store(s, tS, neg) + exp_store(s + 64, tS + 16, neg);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(kPFull + t));
+        }
+
+        // ---------------------------------------------------------------- epilogue
+        if (ok && n_tiles > 0) {
+            ok = wait_bounded(bar(kOFinal + t), 0, wd, ROLE_SOFTMAX, SITE_O_FINAL);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) tc_fence_after();
+        }
+        if (ok) {
+            const bool in_range = row < a.Nq;
+            const int64_t o_off = static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(row) * a.o_sn +
+                                  static_cast<int64_t>(h) * a.o_sh;
+            const int64_t lse_idx = (static_cast<int64_t>(b) * a.H + h) * a.Nq + row;
+            const float c_new = n_tiles > 0 ? a.o_scale / l : 0.f;
+#pragma unroll
+            for (int cc = 0; cc < kD / 32; ++cc) {
+                uint32_t o[32];
+                if (n_tiles > 0) {
+                    tmem_ld32(tO + cc * 32, o);
+                    tmem_ld_wait_dep(o);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                if (in_range) {
+                    if constexpr (OUT_BF16) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + o_off + cc * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * c_new, __uint_as_float(o[8 * v4 + 1]) * c_new);
+                            w.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * c_new, __uint_as_float(o[8 * v4 + 3]) * c_new);
+                            w.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * c_new, __uint_as_float(o[8 * v4 + 5]) * c_new);
+                            w.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * c_new, __uint_as_float(o[8 * v4 + 7]) * c_new);
+                            dst[v4] = w;
+                        }
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + o_off + cc * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4)
+                            dst[v4] = make_float4(__uint_as_float(o[4 * v4 + 0]) * c_new, __uint_as_float(o[4 * v4 + 1]) * c_new,
+                                                  __uint_as_float(o[4 * v4 + 2]) * c_new, __uint_as_float(o[4 * v4 + 3]) * c_new);
+                    }
+                }
+            }
+            if (in_range) a.lse[lse_idx] = n_tiles > 0 ? (m - kPOffset + log2f(l)) * kLn2 : -INFINITY;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <bool BF16>
+cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& args,
+                        int B, cudaStream_t stream) {
+    auto kern = attn_fwd_fp8_kernel<BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((args.Nq + 2 * kBM - 1) / (2 * kBM), args.H, B);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const AttnArgs& args, int B, bool out_bf16, cudaStream_t stream) {
+    return out_bf16 ? launch_impl<true>(tq, tk, tv, args, B, stream) : launch_impl<false>(tq, tk, tv, args, B, stream);
+}
+
+}  // namespace dit

@@ -24,6 +24,7 @@ struct AttnArgs {
     void* out;         // O, fp32 or bf16
     int64_t o_sb, o_sn, o_sh;  // O element strides
     float* lse;        // [B, H, Nq]
+    float o_scale;     // FP8 path: O multiplied by this (descale of V); unused by bf16
     unsigned int* status;      // device status word (4 x u32)
     unsigned long long timeout_ns;
 };
@@ -32,6 +33,11 @@ struct AttnArgs {
 // merge into the fp32 (out, lse) already there instead of overwriting them.
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const AttnArgs& args, int B, int D, bool out_bf16, bool accumulate, cudaStream_t stream);
+
+// FP8 (E4M3) attention forward, D = 128.  Same grid and roles as the bf16
+// kernel; scale_log2 already includes the Q and K descales.
+cudaError_t launch_attn_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const AttnArgs& args, int B, bool out_bf16, cudaStream_t stream);
 
 // Watchdog self-test: one CTA waits on a barrier nothing arrives on.
 cudaError_t launch_watchdog_selftest(unsigned int* status, unsigned long long limit_ns, cudaStream_t stream);
@@ -58,6 +64,19 @@ struct LayoutArgs {
 };
 
 cudaError_t launch_qkv_to_head_major(const LayoutArgs& args, cudaStream_t stream);
+
+struct CastArgs {
+    const uint16_t* qkv;        // bf16 [B, N, 3, H, D], (3, H, D) contiguous
+    int64_t stride_b, stride_n; // elements
+    int N;
+    uint32_t hd;                // H * D (multiple of 16)
+    uint32_t chunks_per_row;    // 3 * H * D / 16
+    uint64_t total_chunks;      // B * N * chunks_per_row (< 2^32)
+    float scale[3];             // q, k, v
+    uint8_t* out;               // E4M3 [B, N, 3, H, D] contiguous
+};
+
+cudaError_t launch_qkv_cast_fp8(const CastArgs& args, cudaStream_t stream);
 
 int device_sm_count(int device);
 

@@ -11,6 +11,9 @@
  *                          disjoint key chunks.
  *   dit_qkv_to_head_major  split of a fused [B, N, 3, H, D] projection
  *                          buffer into three head-major [B, H, N, D] tensors.
+ *   dit_qkv_cast_fp8       one-pass scaled bf16 -> E4M3 cast of that stacked
+ *                          buffer, and dit_attn_fwd_fp8, the attention that
+ *                          reads its output in place.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -173,6 +176,62 @@ dit_status_t dit_qkv_to_head_major(const void *qkv, int64_t stride_b, int64_t st
                                    int B, int N, int H, int D,
                                    void *q_out, void *k_out, void *v_out,
                                    dit_stream_t stream);
+
+/*
+ * dit_qkv_cast_fp8 -- one pass over a stacked bf16 QKV buffer that writes it
+ * as FP8 E4M3 in the same stacked layout, q, k and v each scaled first.
+ *
+ * Defined by "Scaling Video Generation Across NVL72 rack with TensorRT-LLM",
+ * "Ulysses Parallelism", paragraph "Fused vs. unfused QKV all-to-all": the
+ * stacked QKV buffer is one contiguous allocation, so a single FP8 cast covers
+ * all three tensors, and its output goes to the attention kernel without an
+ * intermediate copy.  The pages do not say how the scales are chosen; they are
+ * the caller's (per-tensor factors, e.g. 448 / amax).
+ *
+ * qkv     bf16, element (b, n, t, h, d) at qkv + b*stride_b + n*stride_n +
+ *         (t*H + h)*D + d; stride_b, stride_n multiples of 8 elements; base
+ *         16-byte aligned; D a multiple of 16.
+ * out     E4M3 bytes, [B, N, 3, H, D] contiguous, 16-byte aligned:
+ *         out(b, n, t, h, d) = e4m3(qkv(b, n, t, h, d) * scale_t), the product
+ *         rounded to fp32, then rounded to nearest even E4M3, magnitudes above
+ *         448 saturating to +-448 (NaN stays NaN).
+ * scale_q, scale_k, scale_v  finite and > 0.
+ * DIT_ERR_UNSUPPORTED when 3*H*D > 2^28 or B*N*3*H*D / 16 >= 2^32.
+ */
+dit_status_t dit_qkv_cast_fp8(const void *qkv, int64_t stride_b, int64_t stride_n,
+                              int B, int N, int H, int D,
+                              float scale_q, float scale_k, float scale_v,
+                              void *out, dit_stream_t stream);
+
+/*
+ * dit_attn_fwd_fp8 -- dit_attn_fwd on E4M3 inputs.
+ *
+ * The FP8 attention kernel that the cast above feeds ("Scaling Video
+ * Generation Across NVL72 rack with TensorRT-LLM", "Ulysses Parallelism",
+ * "Fused vs. unfused QKV all-to-all").  q, k, v hold E4M3 codes q8, k8, v8
+ * standing for Q = q8 * descale_q, K = k8 * descale_k, V = v8 * descale_v
+ * (descale = 1 / the cast's scale); the result is dit_attn_fwd's O and LSE
+ * for those Q, K, V.  The probabilities P enter the P.V product as E4M3 (their
+ * largest value per row ~2^7 to 2^8.75), so O carries a relative error of
+ * about 2^-4 / sqrt(number of keys that matter) on top of the inputs'
+ * quantisation; LSE is computed from fp32 P.
+ *
+ * Arguments as dit_attn_fwd, except:
+ * q, k, v   E4M3 bytes; strides in elements (= bytes), the b, n, h strides
+ *           positive multiples of 16.  For the output of dit_qkv_cast_fp8:
+ *           q = out, k = out + H*D, v = out + 2*H*D, strides
+ *           (b, n, h, d) = (N*3*H*D, 3*H*D, D, 1).
+ * D         128 only (DIT_ERR_UNSUPPORTED otherwise).
+ * descale_q, descale_k, descale_v  finite and > 0; scale * descale_q *
+ *           descale_k * log2(e) must lie in (1e-30, 1e30).
+ */
+dit_status_t dit_attn_fwd_fp8(const void *q, const void *k, const void *v,
+                              const dit_attn_strides_t *strides,
+                              int B, int Nq, int Nkv, int H, int D,
+                              int key_valid_len, float scale,
+                              float descale_q, float descale_k, float descale_v,
+                              void *out, dit_dtype_t out_dtype, float *lse,
+                              dit_stream_t stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *dit_status_string(dit_status_t s);

@@ -268,13 +268,16 @@ def e4m3_encode(x) -> np.ndarray:
 def qkv_cast_fp8(qkv_bits: np.ndarray, scales) -> np.ndarray:
     """One-pass cast of a stacked [B, N, 3, H, D] bf16 buffer (uint16 bits) to
     E4M3: out[b, n, t] = e4m3(x[b, n, t] * scales[t]) for t in (q, k, v)."""
-    x = bf16_bits_to_f64(qkv_bits)
-    sc = np.asarray(scales, dtype=np.float64).reshape(1, 1, 3, 1, 1)
-    # the scaled value is formed in fp32 on the device; it is exact in fp32
-    # whenever it is in range (bf16 * fp32 has at most 8 + 24 significant bits,
-    # rounded once), so form it in fp32 here too
-    y = (x.astype(np.float32) * sc.astype(np.float32)).astype(np.float64)
-    return e4m3_encode(y)
+    bits = np.asarray(qkv_bits, dtype=np.uint16)
+    sc = np.asarray(scales, dtype=np.float32).reshape(1, 1, 3, 1, 1)
+    out = np.empty(bits.shape, dtype=np.uint8)
+    step = max(1, (1 << 22) // max(1, int(np.prod(bits.shape[2:]))))   # rows per slice, bounds the temporaries
+    for n0 in range(0, bits.shape[1], step):
+        x = bf16_bits_to_f64(bits[:, n0:n0 + step]).astype(np.float32)
+        # the scaled value is formed in fp32 on the device: one fp32 rounding of
+        # the product, then one E4M3 rounding; the same two roundings here
+        out[:, n0:n0 + step] = e4m3_encode((x * sc).astype(np.float64))
+    return out
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
@@ -295,9 +298,8 @@ def attn_fp8(q8: np.ndarray, k8: np.ndarray, v8: np.ndarray, *, scale: float, de
     """Attention on E4M3 inputs q8, k8, v8 ([B, N, H, D] uint8 views) that stand
     for Q = q8 * descale_q, K = k8 * descale_k, V = v8 * descale_v:
     softmax(scale * Q K^T) V and its LSE, in fp64, through ``attn``."""
-    qb = e4m3_to_bf16_bits(q8)
-    kb = e4m3_to_bf16_bits(k8)
-    vb = e4m3_to_bf16_bits(v8)
+    lut = e4m3_to_bf16_bits(np.arange(256, dtype=np.uint8))
+    qb, kb, vb = (lut[np.asarray(a, dtype=np.uint8)] for a in (q8, k8, v8))
     O, L = attn(qb, kb, vb, key_valid_len=key_valid_len, scale=scale * descale_q * descale_k, rows=rows,
                 threads=threads)
     return O * descale_v, L

@@ -69,3 +69,30 @@ def compare(O_gpu: np.ndarray, L_gpu: np.ndarray, O_ref: np.ndarray, L_ref: np.n
         res["o_rel_l2"] = rel
         assert rel <= rel_l2, res
     return res
+
+
+# ---------------------------------------------------------------- FP8 path
+# The FP8 kernel rounds each probability P to E4M3 before the P.V product
+# (relative rounding error |delta| <= 2^-4 for the normal range; P's row max
+# is >= 2^7 so subnormal P are >= 2^-16 below it).  Against the fp64 oracle
+# on the same E4M3 inputs:
+#   |O - O_ref| = |sum_j P_j delta_j v_j| / sum_j P_j <= 2^-4 * max_j |v_j|,
+# the hard per-element bound (plus 1e-3 for the fp32 arithmetic); and, delta
+# being zero-mean with RMS 2^-4 * sqrt(E[1/m^2] / 3) ~= 0.027 over mantissas
+# m in [1, 2), the per-head relative L2 error of O is ~0.027 -- gated at 0.04.
+# LSE comes from the unrounded fp32 P: the bf16 gate (1e-3) applies.
+FP8_O_REL_L2 = 0.04
+
+
+def compare_fp8(O_gpu, L_gpu, O_ref, L_ref, v_absmax: float, head_axes=(0, 1)):
+    return compare(O_gpu, L_gpu, O_ref, L_ref, head_axes=head_axes, o_max=2.0 ** -4 * v_absmax + 1e-3,
+                   o_mean=float("inf"), lse_max=LSE_MAX_ABS, rel_l2=FP8_O_REL_L2)
+
+
+def host_u8(t: torch.Tensor) -> np.ndarray:
+    """Host copy of a (possibly strided) uint8 device view, strides kept."""
+    if t.device.type == "cpu":
+        return t.numpy()
+    n = t.untyped_storage().nbytes()
+    base = torch.empty(0, dtype=torch.uint8, device=t.device).set_(t.untyped_storage(), 0, (n,), (1,))
+    return base.cpu().as_strided(t.shape, t.stride(), t.storage_offset()).numpy()

@@ -120,3 +120,53 @@ def test_product_path_never_imports_oracle():
                 text = open(os.path.join(dirpath, fn), encoding="utf-8").read()
                 assert "import oracle" not in text and "from oracle" not in text, fn
                 assert "attn_oracle" not in text, fn
+
+
+def _fwd8(lib, **kw):
+    g = lib.Strides4(8 * 3 * 4 * 128, 3 * 4 * 128, 128, 1)       # views of a stacked E4M3 buffer
+    o = lib.Strides4(8 * 128 * 4, 4 * 128, 128, 1)
+    args = dict(q=FAKE, k=FAKE + 512, v=FAKE + 1024, st=lib.AttnStrides(g, g, g, o), B=1, Nq=8, Nkv=8, H=4, D=128,
+                kvl=8, scale=0.088, dq=0.01, dk=0.01, dv=0.02, out=FAKE, dt=lib.DIT_BF16, lse=FAKE)
+    args.update(kw)
+    return lib.raw().dit_attn_fwd_fp8(args["q"], args["k"], args["v"], ctypes.byref(args["st"]), args["B"],
+                                      args["Nq"], args["Nkv"], args["H"], args["D"], args["kvl"], args["scale"],
+                                      args["dq"], args["dk"], args["dv"], args["out"], args["dt"], args["lse"], None)
+
+
+def test_attn_fwd_fp8_argument_checks(lib):
+    E = lib
+    assert _fwd8(lib, D=64) == E.DIT_ERR_UNSUPPORTED            # head dim 128 only
+    assert _fwd8(lib, dq=0.0) == E.DIT_ERR_INVALID_ARG
+    assert _fwd8(lib, dk=-1.0) == E.DIT_ERR_INVALID_ARG
+    assert _fwd8(lib, dv=float("inf")) == E.DIT_ERR_INVALID_ARG
+    assert _fwd8(lib, dv=float("nan")) == E.DIT_ERR_INVALID_ARG
+    assert _fwd8(lib, dq=1e-20, dk=1e-20) == E.DIT_ERR_INVALID_ARG   # folded exponent scale underflows
+    assert _fwd8(lib, kvl=9) == E.DIT_ERR_INVALID_ARG
+    assert _fwd8(lib, q=FAKE + 8) == E.DIT_ERR_ALIGNMENT
+    g8 = lib.Strides4(8 * 3 * 4 * 128, 3 * 4 * 128 + 8, 128, 1)   # 8 bytes: fine for bf16, not for E4M3 TMA
+    g = lib.Strides4(8 * 3 * 4 * 128, 3 * 4 * 128, 128, 1)
+    o = lib.Strides4(8 * 128 * 4, 4 * 128, 128, 1)
+    assert _fwd8(lib, st=lib.AttnStrides(g, g8, g, o)) == E.DIT_ERR_ALIGNMENT
+    assert _fwd8(lib, B=0, q=None, out=None, lse=None) == E.DIT_OK
+
+
+def test_cast_fp8_argument_checks(lib):
+    f = lib.raw().dit_qkv_cast_fp8
+    ok = (FAKE, 0, 3 * 4 * 64, 1, 8, 4, 64, 1.0, 2.0, 3.0, FAKE, None)
+
+    def call(**kw):
+        a = list(ok)
+        names = ["qkv", "sb", "sn", "B", "N", "H", "D", "sq", "sk", "sv", "out", "s"]
+        for k_, v_ in kw.items():
+            a[names.index(k_)] = v_
+        return f(*a)
+    assert call(D=8, sn=3 * 4 * 8) == lib.DIT_ERR_UNSUPPORTED       # D % 16
+    assert call(sq=0.0) == lib.DIT_ERR_INVALID_ARG
+    assert call(sv=float("inf")) == lib.DIT_ERR_INVALID_ARG
+    assert call(sk=float("nan")) == lib.DIT_ERR_INVALID_ARG
+    assert call(sn=3 * 4 * 64 + 4) == lib.DIT_ERR_ALIGNMENT
+    assert call(out=FAKE + 8) == lib.DIT_ERR_ALIGNMENT
+    assert call(qkv=None) == lib.DIT_ERR_INVALID_ARG
+    assert call(N=-1) == lib.DIT_ERR_INVALID_ARG
+    assert call(B=4, N=1 << 20, H=64, D=128, sn=3 * 64 * 128) == lib.DIT_ERR_UNSUPPORTED   # >= 2^32 chunks
+    assert call(N=0) == lib.DIT_OK
