@@ -303,3 +303,51 @@ def attn_fp8(q8: np.ndarray, k8: np.ndarray, v8: np.ndarray, *, scale: float, de
     O, L = attn(qb, kb, vb, key_valid_len=key_valid_len, scale=scale * descale_q * descale_k, rows=rows,
                 threads=threads)
     return O * descale_v, L
+
+
+# ------------------------------------------------- Q/K normalisation + RoPE
+# "CUDA IPC Ulysses：在 H100 上重叠 Attention 通信", "基线与瓶颈": Q and K are
+# normalised and rotated (RoPE) before attention, V is not; the pages give
+# neither formula.  Reading taken here: RMSNorm over the head dimension,
+#     y_d = x_d / sqrt(mean_d(x_d^2) + eps) * w_d,
+# then the RoFormer rotation of consecutive pairs by per-position angles whose
+# cosines and sines the caller tabulates ([N, D/2]; 1-D or 3-D positions alike):
+#     (y_2i, y_2i+1) -> (y_2i c - y_2i+1 s,  y_2i s + y_2i+1 c),  c, s = cos/sin[n, i].
+
+def rms_norm(x: np.ndarray, weight, eps: float) -> np.ndarray:
+    """RMSNorm over the last axis in fp64; weight None = no scaling."""
+    x = np.asarray(x, dtype=np.float64)
+    y = x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return y if weight is None else y * np.asarray(weight, dtype=np.float64)
+
+
+def rope_pairs(y: np.ndarray, cos: np.ndarray, sin: np.ndarray) -> np.ndarray:
+    """Rotate consecutive pairs of the last axis; cos/sin broadcast against
+    y[..., 0::2] (e.g. [N, 1, D/2] against [N, H, D/2])."""
+    y = np.asarray(y, dtype=np.float64)
+    c = np.asarray(cos, dtype=np.float64)
+    s = np.asarray(sin, dtype=np.float64)
+    out = np.empty_like(y)
+    a, b = y[..., 0::2], y[..., 1::2]
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = a * s + b * c
+    return out
+
+
+def qkv_norm_rope_to_head_major(qkv_bits: np.ndarray, q_weight, k_weight, eps: float, rope_cos, rope_sin):
+    """Fused [B, N, 3, H, D] bf16 (uint16 bits) -> fp64 head-major q, k, v
+    [B, H, N, D]: q and k RMS-normalised (weight None = no norm for that tensor)
+    and rotated (tables None = no rotation), v copied."""
+    x = bf16_bits_to_f64(qkv_bits)
+    outs = []
+    for t, w in ((0, q_weight), (1, k_weight), (2, None)):
+        y = x[:, :, t]                                    # [B, N, H, D]
+        if t < 2:
+            if w is not None:
+                y = rms_norm(y, w, eps)
+            if rope_cos is not None:
+                c = np.asarray(rope_cos, dtype=np.float64)[None, :, None, :]
+                s = np.asarray(rope_sin, dtype=np.float64)[None, :, None, :]
+                y = rope_pairs(y, c, s)
+        outs.append(np.ascontiguousarray(np.transpose(y, (0, 2, 1, 3))))
+    return tuple(outs)
