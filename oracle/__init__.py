@@ -84,7 +84,7 @@ def bind_library(path: str):
                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                   ctypes.c_double, ctypes.c_int, ctypes.c_int,
                   ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
-                  ctypes.c_int]
+                  ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64]
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
 
@@ -115,7 +115,7 @@ def _bf16_view_strides(a: np.ndarray, name: str):
 
 def attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, key_valid_len: int | None = None,
          scale: float | None = None, rows: np.ndarray | None = None, threads: int = 0,
-         lib=None):
+         lib=None, allow: np.ndarray | None = None):
     """fp64 attention with LSE on bf16 inputs given as uint16 bit arrays.
 
     q: [B, Nq, H, D], k/v: [B, Nkv, H, D] -- any numpy views (strided views
@@ -124,8 +124,11 @@ def attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, key_valid_len: int | No
     rows None  -> every query row; returns O [B, Nq, H, D], LSE [B, H, Nq].
     rows given -> an int array [B, H, R] of query rows per head; returns
                   O [B, H, R, D] and LSE [B, H, R] for those rows.
-    Keys j >= key_valid_len are masked (default: none).  ``lib`` selects another
-    compiled copy of the oracle (the mutation tests use it).
+    Keys j >= key_valid_len are masked (default: none).  ``allow`` (optional,
+    [B, Nq, >= key_valid_len], bool or uint8, last axis contiguous): query i
+    may attend key j only where allow[b, i, j]; rows left with no key give
+    O = 0, LSE = -inf.  ``lib`` selects another compiled copy of the oracle
+    (the mutation tests use it).
     """
     lib = _load() if lib is None else lib
     B, Nq, H, D = q.shape
@@ -142,6 +145,15 @@ def attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, key_valid_len: int | No
     R = rows.shape[2]
     o = np.empty((B, H, R, D), dtype=np.float64)
     lse = np.empty((B, H, R), dtype=np.float64)
+    al_ptr, al_sb, al_si = None, 0, 0
+    if allow is not None:
+        allow = np.asarray(allow)
+        if allow.dtype == np.bool_:
+            allow = allow.view(np.uint8)
+        if allow.dtype != np.uint8 or allow.ndim != 3 or allow.shape[0] != B or allow.shape[1] != Nq \
+                or allow.shape[2] < kvl or allow.strides[2] != 1:
+            raise ValueError("allow must be a [B, Nq, >= key_valid_len] byte array, last axis contiguous")
+        al_ptr, al_sb, al_si = allow.ctypes.data, allow.strides[0], allow.strides[1]
     for b in range(B):
         for h in range(H):
             r_bh = np.ascontiguousarray(rows[b, h])
@@ -149,7 +161,8 @@ def attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, key_valid_len: int | No
             l_bh = np.empty((R,), dtype=np.float64)
             rc = lib.oracle_attn_head_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, qs, ks, vs,
                                            Nq, Nkv, D, kvl, sc, b, h, r_bh.ctypes.data, R,
-                                           o_bh.ctypes.data, l_bh.ctypes.data, int(threads))
+                                           o_bh.ctypes.data, l_bh.ctypes.data, int(threads),
+                                           al_ptr, al_sb, al_si)
             if rc != 0:
                 raise ValueError(f"oracle_attn_head_rows failed with {rc}")
             o[b, h] = o_bh
@@ -351,3 +364,17 @@ def qkv_norm_rope_to_head_major(qkv_bits: np.ndarray, q_weight, k_weight, eps: f
                 y = rope_pairs(y, c, s)
         outs.append(np.ascontiguousarray(np.transpose(y, (0, 2, 1, 3))))
     return tuple(outs)
+
+
+def expand_mask(mask: np.ndarray, n_padded: int) -> np.ndarray:
+    """The padding rule of "8 卡怎么分 token", "构造 padding mask", for a user
+    (B, T, T) mask (True = may attend): expanded to (B, Tp, Tp), pad key
+    columns j >= T are masked and pad query rows i >= T attend every valid key."""
+    mask = np.asarray(mask, dtype=bool)
+    B, T, T2 = mask.shape
+    if T != T2 or n_padded < T:
+        raise ValueError("mask must be (B, T, T) with T <= n_padded")
+    out = np.zeros((B, n_padded, n_padded), dtype=bool)
+    out[:, :T, :T] = mask
+    out[:, T:, :T] = True
+    return out

@@ -9,7 +9,7 @@
  *
  * What it computes (one (b, h) head, a caller-chosen list of query rows i):
  *
- *     J      = { j : 0 <= j < key_valid_len }            (key-only mask)
+ *     J      = { j : 0 <= j < key_valid_len, allow[b,i,j] }  (allow optional)
  *     s_ij   = scale * sum_d q[b,i,h,d] * k[b,j,h,d]       (fp64)
  *     m_i    = max_{j in J} s_ij
  *     l_i    = sum_{j in J} exp(s_ij - m_i)
@@ -38,6 +38,10 @@
  *     that an empty key chunk has weight zero in a merge.
  *   - Masked keys are the tail j >= key_valid_len (pads are appended at the end
  *     of the sequence and cut again after the gather).
+ *   - A general (B, T, T) mask (same page, same paragraph: a user mask is
+ *     expanded over the pad rows and columns) enters as `allow`, one byte per
+ *     (b, i, j), 1 = may attend; a row whose J is empty gets O = 0, LSE = -inf
+ *     (where a plain softmax would produce NaN).
  *
  * Inputs are bf16 bit patterns; each converts exactly to double.
  */
@@ -63,6 +67,8 @@ static float bf16_bits_to_float(uint16_t bits) {
  *
  * q, k, v          : base pointers to bf16 bit patterns.
  * q_s, k_s, v_s    : element strides {b, n, h}; d is contiguous.
+ * allow            : NULL, or bytes with allow[b*allow_sb + i*allow_si + j] != 0
+ *                    when query i may attend key j (j < key_valid_len).
  * o_out            : n_rows x D doubles, row r is query rows[r].
  * lse_out          : n_rows doubles.
  * Returns 0, or -1 when an argument is out of range, -2 on allocation failure.
@@ -71,7 +77,8 @@ int oracle_attn_head_rows(const uint16_t *q, const uint16_t *k, const uint16_t *
                           const int64_t *q_s, const int64_t *k_s, const int64_t *v_s,
                           int Nq, int Nkv, int D, int key_valid_len, double scale,
                           int b, int h, const int32_t *rows, int n_rows,
-                          double *o_out, double *lse_out, int n_threads) {
+                          double *o_out, double *lse_out, int n_threads,
+                          const uint8_t *allow, int64_t allow_sb, int64_t allow_si) {
     if (D <= 0 || Nq < 0 || Nkv < 0 || key_valid_len < 0 || key_valid_len > Nkv || n_rows < 0)
         return -1;
     for (int r = 0; r < n_rows; ++r)
@@ -120,19 +127,27 @@ int oracle_attn_head_rows(const uint16_t *q, const uint16_t *k, const uint16_t *
                 const uint16_t *qr = q + (int64_t)b * q_s[0] + (int64_t)i * q_s[1] + (int64_t)h * q_s[2];
                 for (int d = 0; d < D; ++d) qd[d] = (double)bf16_bits_to_float(qr[d]);
 
-                /* pass 1: scores and their maximum */
+                /* pass 1: scores of the allowed keys and their maximum */
+                const uint8_t *al = allow ? allow + (int64_t)b * allow_sb + (int64_t)i * allow_si : NULL;
                 double m = -INFINITY;
                 for (int j = 0; j < nj; ++j) {
+                    if (al && !al[j]) { s[j] = -INFINITY; continue; }
                     const float *kj = kh + (int64_t)j * D;
                     double dot = 0.0;
                     for (int d = 0; d < D; ++d) dot += qd[d] * (double)kj[d];
                     s[j] = scale * dot;
                     if (s[j] > m) m = s[j];
                 }
+                if (m == -INFINITY) {          /* no allowed key */
+                    for (int d = 0; d < D; ++d) o_out[(int64_t)r * D + d] = 0.0;
+                    lse_out[r] = -INFINITY;
+                    continue;
+                }
                 /* pass 2: normaliser and weighted sum of values */
                 double l = 0.0;
                 for (int d = 0; d < D; ++d) acc[d] = 0.0;
                 for (int j = 0; j < nj; ++j) {
+                    if (s[j] == -INFINITY) continue;
                     const double p = exp(s[j] - m);
                     const float *vj = vh + (int64_t)j * D;
                     l += p;

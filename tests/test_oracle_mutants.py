@@ -31,6 +31,10 @@ MUTANTS = {
     "exponent_sign": ("const double p = exp(s[j] - m);", "const double p = exp(m - s[j]);"),
     "channel_index_slip": ("dot += qd[d] * (double)kj[d];", "dot += qd[d] * (double)kj[(d + 1) % D];"),
     "log2_instead_of_ln": ("lse_out[r] = m + log(l);", "lse_out[r] = m + log2(l);"),
+    "allow_mask_ignored": ("if (al && !al[j]) { s[j] = -INFINITY; continue; }", "if (0) { continue; }"),
+    "allow_mask_inverted": ("if (al && !al[j])", "if (al && al[j])"),
+    "allow_mask_wrong_row": ("(int64_t)i * allow_si", "(int64_t)(i + 1 < Nq ? i + 1 : i) * allow_si"),
+    "empty_row_not_zero": ("if (m == -INFINITY) {          /* no allowed key */", "if (0) {"),
 }
 
 
@@ -59,6 +63,31 @@ def _pin_suite(lib):
     if not (np.allclose(O, ref.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-12)
             and np.allclose(L, lref.numpy(), rtol=0, atol=1e-12)):
         failures.append("sdpa_fp64")
+
+    # library special case: a general boolean mask (fp64 SDPA), one row fully masked
+    g = torch.Generator().manual_seed(5)
+    Bm, Nm, Hm, Dm = 2, 24, 2, 32
+    qm, km, vm, _ = wl.make_qkv(Bm, Nm, Hm, Dm, seed=33)
+    allow = torch.rand((Bm, Nm, Nm), generator=g) < 0.4
+    allow[:, :, 0] = True
+    allow[1, 5, :] = False
+    try:
+        Om, Lm = oracle.attn(bits(qm), bits(km), bits(vm), scale=0.2, allow=allow.numpy(), lib=lib)
+    except Exception:
+        return failures + ["raised_mask"]
+    qt, kt, vt = (x.to(torch.float64).permute(0, 2, 1, 3) for x in (qm, km, vm))
+    am = allow[:, None]
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=am, scale=0.2)
+    s_ = 0.2 * torch.einsum("bhid,bhjd->bhij", qt, kt)
+    lref = torch.logsumexp(s_.masked_fill(~am, -float("inf")), -1)
+    ref = ref.permute(0, 2, 1, 3).numpy()
+    ok_rows = np.ones((Bm, Nm), dtype=bool)
+    ok_rows[1, 5] = False
+    if not (np.allclose(Om[ok_rows], ref[ok_rows], rtol=0, atol=1e-12)
+            and np.allclose(Lm.transpose(0, 2, 1)[ok_rows], lref.permute(0, 2, 1).numpy()[ok_rows], rtol=0,
+                            atol=1e-12)
+            and np.all(Om[1, 5] == 0) and np.all(np.isneginf(Lm[1, :, 5]))):
+        failures.append("sdpa_fp64_general_mask")
 
     # closed form: weights 1:2:4 -> O = (5, 6), LSE = ln 7
     def exact(arr):
