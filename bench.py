@@ -339,6 +339,34 @@ def time_layout_kernel(step, reps=5):
     return nbytes, statistics.median(ts)
 
 
+def time_norm_rope_kernel(step, reps=5):
+    """HBM roofline of the split with Q/K RMSNorm + 3-D RoPE fused in (2 + 2
+    bytes per element; the fp32 angle tables are read from L2)."""
+    import torch
+    from dit_long_sequence_gb300 import workloads as wl
+    if step.mode != "layout+attn":
+        return None
+    w = step.w
+    grid = {24576: (16, 32, 48), 1024: (4, 16, 16)}.get(w.N)
+    if grid is None:
+        return None
+    cos, sin = wl.rope_tables_3d(grid, w.D, device=step.dev)
+    wq = torch.ones((w.D,), device=step.dev)
+    wk = torch.ones((w.D,), device=step.dev)
+    s = step.stream
+    ts = []
+    for i in range(reps + 2):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        step.dl.qkv_norm_rope_to_head_major(step.inputs[0], q_weight=wq, k_weight=wk, rope_cos=cos, rope_sin=sin,
+                                            outs=step.planes, stream=s)
+        b.record(s)
+        b.synchronize()
+        if i >= 2:
+            ts.append(a.elapsed_time(b))
+    return 2 * step.inputs[0].numel() * 2, statistics.median(ts)
+
+
 # --------------------------------------------------------------- cpu baseline
 
 def cpu_baseline(w, dev_inputs=None, target_s=12.0):
@@ -528,6 +556,11 @@ def main(argv=None):
     if lay is not None:
         gbs = lay[0] / (lay[1] * 1e-3) / 1e9
         extra["cast_fp8" if w.fp8 else "layout"] = {"bytes": lay[0], "ms": lay[1], "GB/s": gbs, "frac_hbm": gbs / float(peaks["hbm_gbs"])}
+    nr = time_norm_rope_kernel(step)
+    if nr is not None:
+        gbs = nr[0] / (nr[1] * 1e-3) / 1e9
+        extra["layout_norm_rope"] = {"bytes": nr[0], "ms": nr[1], "GB/s": gbs,
+                                     "frac_hbm": gbs / float(peaks["hbm_gbs"])}
     for il, key in ((True, "merge_n9_interleaved"), (False, "merge_n9_chunk_major")):
         mb, mms = time_merge_kernel(dev, w.B, w.N, w.H, w.D, n_chunks=9, interleaved=il)
         mgbs = mb / (mms * 1e-3) / 1e9

@@ -44,11 +44,17 @@ _lib.dit_attn_fwd.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i
 _lib.dit_attn_fwd_accumulate.restype = _i
 _lib.dit_attn_fwd_accumulate.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
                                          _vp, _vp, _vp]
+_lib.dit_attn_fwd_masked.restype = _i
+_lib.dit_attn_fwd_masked.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _vp, _i64,
+                                     _i64, _i, _f, _vp, _i, _vp, _vp]
 _lib.dit_attn_fwd_fp8.restype = _i
 _lib.dit_attn_fwd_fp8.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f, _f, _f, _f,
                                   _vp, _i, _vp, _vp]
 _lib.dit_qkv_cast_fp8.restype = _i
 _lib.dit_qkv_cast_fp8.argtypes = [_vp, _i64, _i64, _i, _i, _i, _i, _f, _f, _f, _vp, _vp]
+_lib.dit_qkv_norm_rope_to_head_major.restype = _i
+_lib.dit_qkv_norm_rope_to_head_major.argtypes = [_vp, _i64, _i64, _i, _i, _i, _i, _vp, _vp, _f, _vp, _vp, _vp, _vp,
+                                                 _vp, _vp]
 _lib.dit_watchdog_selftest.restype = _i
 _lib.dit_watchdog_selftest.argtypes = [ctypes.c_uint32, _vp]
 _lib.dit_attn_lse_merge.restype = _i
@@ -61,8 +67,9 @@ _lib.dit_check_watchdog.restype = _i
 _lib.dit_check_watchdog.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
 _lib.dit_version.restype = ctypes.c_uint32
 
-EXPORTS = ("dit_attn_fwd", "dit_attn_fwd_accumulate", "dit_attn_lse_merge", "dit_qkv_to_head_major",
-           "dit_qkv_cast_fp8", "dit_attn_fwd_fp8", "dit_status_string", "dit_check_watchdog",
+EXPORTS = ("dit_attn_fwd", "dit_attn_fwd_masked", "dit_attn_fwd_accumulate", "dit_attn_lse_merge", "dit_qkv_to_head_major",
+           "dit_qkv_norm_rope_to_head_major", "dit_qkv_cast_fp8", "dit_attn_fwd_fp8", "dit_status_string",
+           "dit_check_watchdog",
            "dit_watchdog_selftest", "dit_version")
 
 
@@ -122,6 +129,51 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, key_valid_len
                            sc, out.data_ptr(), DIT_F32 if out.dtype == torch.float32 else DIT_BF16,
                            lse.data_ptr(), _stream_ptr(stream))
     _check(rc, "dit_attn_fwd")
+    return out, lse
+
+
+def attn_fwd_masked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_bits: torch.Tensor, *,
+                    mask_rows: int | None = None, key_valid_len: int | None = None, scale: float | None = None,
+                    out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                    out_dtype: torch.dtype = torch.float32, stream=None):
+    """Attention with a general bit mask through `dit_attn_fwd_masked`.
+
+    mask_bits: int32 CUDA tensor [B or 1, R, W] of packed bits (bit j&31 of word
+    j>>5 of row i: query i may attend key j), W a multiple of 4 with
+    W >= 4*ceil(key_valid_len/128); a leading dimension of 1 shares the mask
+    across the batch.  Rows i >= mask_rows (default R) attend every valid key.
+    """
+    B, Nq, H, D = q.shape
+    Nkv = k.shape[1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a bf16 CUDA tensor")
+    if k.shape != (B, Nkv, H, D) or v.shape != (B, Nkv, H, D):
+        raise ValueError("k and v must be [B, Nkv, H, D] matching q")
+    if mask_bits.dtype != torch.int32 or mask_bits.dim() != 3 or mask_bits.stride(2) != 1 or not mask_bits.is_cuda:
+        raise ValueError("mask_bits must be an int32 CUDA tensor [B or 1, rows, words], words contiguous")
+    if mask_bits.shape[0] not in (1, B):
+        raise ValueError("mask_bits must have B or 1 batch entries")
+    rows = mask_bits.shape[1] if mask_rows is None else int(mask_rows)
+    if rows > mask_bits.shape[1]:
+        raise ValueError("mask_rows exceeds the mask's rows")
+    kvl = Nkv if key_valid_len is None else int(key_valid_len)
+    sc = float(D) ** -0.5 if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, Nq, H, D), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if out.dtype not in (torch.float32, torch.bfloat16) or tuple(out.shape) != (B, Nq, H, D):
+        raise ValueError("out must be a [B, Nq, H, D] fp32 or bf16 tensor")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
+    sb = 0 if mask_bits.shape[0] == 1 else mask_bits.stride(0)
+    st = AttnStrides(_strides4(q), _strides4(k), _strides4(v), _strides4(out))
+    rc = _lib.dit_attn_fwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(st), B, Nq, Nkv, H, D, kvl,
+                                  mask_bits.data_ptr(), sb, mask_bits.stride(1), rows, sc, out.data_ptr(),
+                                  DIT_F32 if out.dtype == torch.float32 else DIT_BF16, lse.data_ptr(),
+                                  _stream_ptr(stream))
+    _check(rc, "dit_attn_fwd_masked")
     return out, lse
 
 
@@ -200,6 +252,42 @@ def qkv_to_head_major(qkv: torch.Tensor, *, outs=None, stream=None):
                                     outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(),
                                     _stream_ptr(stream))
     _check(rc, "dit_qkv_to_head_major")
+    return outs
+
+
+def qkv_norm_rope_to_head_major(qkv: torch.Tensor, *, q_weight: torch.Tensor | None = None,
+                                k_weight: torch.Tensor | None = None, eps: float = 1e-6,
+                                rope_cos: torch.Tensor | None = None, rope_sin: torch.Tensor | None = None,
+                                outs=None, stream=None):
+    """dit_qkv_to_head_major with Q/K RMSNorm (fp32 [D] weights; None skips)
+    and RoPE on consecutive pairs (fp32 [N, D/2] cos/sin tables; None skips)
+    fused in, through `dit_qkv_norm_rope_to_head_major`."""
+    B, N, three, H, D = qkv.shape
+    if three != 3 or qkv.dtype != torch.bfloat16 or not qkv.is_cuda:
+        raise ValueError("expected a bf16 CUDA [B, N, 3, H, D] tensor")
+    if qkv.stride(4) != 1 or qkv.stride(3) != D or qkv.stride(2) != H * D:
+        raise ValueError("the [3, H, D] block of every sequence row must be contiguous")
+    for name, w in (("q_weight", q_weight), ("k_weight", k_weight)):
+        if w is not None and (w.dtype != torch.float32 or tuple(w.shape) != (D,) or not w.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous fp32 [D] tensor")
+    if (rope_cos is None) != (rope_sin is None):
+        raise ValueError("pass both rope tables or neither")
+    for name, tb in (("rope_cos", rope_cos), ("rope_sin", rope_sin)):
+        if tb is not None and (tb.dtype != torch.float32 or tuple(tb.shape) != (N, D // 2) or not tb.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous fp32 [N, D/2] tensor")
+    if outs is None:
+        outs = tuple(torch.empty((B, H, N, D), dtype=torch.bfloat16, device=qkv.device) for _ in range(3))
+    for o in outs:
+        if not o.is_contiguous() or tuple(o.shape) != (B, H, N, D) or o.dtype != torch.bfloat16:
+            raise ValueError("outputs must be contiguous bf16 [B, H, N, D]")
+
+    def ptr(t):
+        return None if t is None else t.data_ptr()
+    rc = _lib.dit_qkv_norm_rope_to_head_major(qkv.data_ptr(), qkv.stride(0), qkv.stride(1), B, N, H, D,
+                                              ptr(q_weight), ptr(k_weight), float(eps), ptr(rope_cos),
+                                              ptr(rope_sin), outs[0].data_ptr(), outs[1].data_ptr(),
+                                              outs[2].data_ptr(), _stream_ptr(stream))
+    _check(rc, "dit_qkv_norm_rope_to_head_major")
     return outs
 
 

@@ -117,11 +117,18 @@ extern "C" {
 
 namespace {
 
+struct MaskSpec {
+    const uint32_t* bits;
+    int64_t batch_stride, row_stride;   // in 32-bit words
+    int rows;
+};
+
 // fp8: E4M3 inputs (D = 128 only), descales[3] = (q, k, v); otherwise bf16.
+// mask: the general bit mask of dit_attn_fwd_masked (bf16 only).
 dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides, int B,
                              int Nq, int Nkv, int H, int D, int key_valid_len, float scale, void* out,
                              dit_dtype_t out_dtype, float* lse, bool accumulate, dit_stream_t stream,
-                             const float* descales = nullptr) {
+                             const float* descales = nullptr, const MaskSpec* mask = nullptr) {
     const bool fp8 = descales != nullptr;
     if (strides == nullptr) return DIT_ERR_INVALID_ARG;
     if (B < 0 || Nq < 0 || Nkv < 0 || H < 0) return DIT_ERR_INVALID_ARG;
@@ -175,6 +182,15 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
     a.n_kv_tiles = (key_valid_len + 127) / 128;
     a.scale_log2 = static_cast<float>(sl2);
     a.o_scale = fp8 ? descales[2] : 1.f;
+    a.mask = nullptr;
+    a.mask_sb = a.mask_si = 0;
+    a.mask_rows = 0;
+    if (mask != nullptr && mask->rows > 0 && any_keys) {
+        a.mask = mask->bits;
+        a.mask_sb = mask->batch_stride;
+        a.mask_si = mask->row_stride;
+        a.mask_rows = mask->rows;
+    }
     a.out = out;
     a.o_sb = so.b;
     a.o_sn = so.n;
@@ -206,6 +222,22 @@ dit_status_t dit_attn_fwd_accumulate(const void* q, const void* k, const void* v
                                      float* lse, dit_stream_t stream) {
     return attn_fwd_common(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, scale, out, DIT_F32, lse, true,
                            stream);
+}
+
+dit_status_t dit_attn_fwd_masked(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides,
+                                 int B, int Nq, int Nkv, int H, int D, int key_valid_len, const uint32_t* mask,
+                                 int64_t mask_batch_stride, int64_t mask_row_stride, int mask_rows, float scale,
+                                 void* out, dit_dtype_t out_dtype, float* lse, dit_stream_t stream) {
+    if (mask_rows < 0 || mask_rows > Nq) return DIT_ERR_INVALID_ARG;
+    if (mask_rows > 0) {
+        if (mask == nullptr) return DIT_ERR_INVALID_ARG;
+        const int64_t words_read = 4 * static_cast<int64_t>((key_valid_len + 127) / 128);
+        if (mask_row_stride < words_read || mask_batch_stride < 0) return DIT_ERR_INVALID_ARG;
+        if (mask_row_stride % 4 || mask_batch_stride % 4 || !aligned16(mask)) return DIT_ERR_ALIGNMENT;
+    }
+    const MaskSpec spec{mask, mask_batch_stride, mask_row_stride, mask_rows};
+    return attn_fwd_common(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, scale, out, out_dtype, lse, false,
+                           stream, nullptr, &spec);
 }
 
 dit_status_t dit_attn_fwd_fp8(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides,
@@ -307,6 +339,43 @@ dit_status_t dit_qkv_to_head_major(const void* qkv, int64_t stride_b, int64_t st
     a.out[1] = static_cast<uint16_t*>(k_out);
     a.out[2] = static_cast<uint16_t*>(v_out);
     cudaError_t e = launch_qkv_to_head_major(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DIT_OK : DIT_ERR_CUDA;
+}
+
+dit_status_t dit_qkv_norm_rope_to_head_major(const void* qkv, int64_t stride_b, int64_t stride_n, int B, int N,
+                                             int H, int D, const float* q_weight, const float* k_weight, float eps,
+                                             const float* rope_cos, const float* rope_sin, void* q_out, void* k_out,
+                                             void* v_out, dit_stream_t stream) {
+    if (B < 0 || N < 0 || H < 0 || D < 0) return DIT_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return DIT_ERR_INVALID_ARG;
+    if ((rope_cos == nullptr) != (rope_sin == nullptr)) return DIT_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return DIT_ERR_UNSUPPORTED;
+    if (B == 0 || N == 0 || H == 0) return DIT_OK;
+    if (qkv == nullptr || q_out == nullptr || k_out == nullptr || v_out == nullptr) return DIT_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(3) * H * D > (int64_t(1) << 28)) return DIT_ERR_UNSUPPORTED;
+    if (stride_b < 0 || stride_n < 0) return DIT_ERR_INVALID_ARG;
+    if (stride_b % 8 || stride_n % 8) return DIT_ERR_ALIGNMENT;
+    if (!aligned16(qkv) || !aligned16(q_out) || !aligned16(k_out) || !aligned16(v_out)) return DIT_ERR_ALIGNMENT;
+    if ((q_weight && !aligned16(q_weight)) || (k_weight && !aligned16(k_weight)) ||
+        (rope_cos && (!aligned16(rope_cos) || !aligned16(rope_sin))))
+        return DIT_ERR_ALIGNMENT;
+    NormRopeArgs a;
+    a.qkv = static_cast<const uint16_t*>(qkv);
+    a.stride_b = stride_b;
+    a.stride_n = stride_n;
+    a.B = B;
+    a.N = N;
+    a.H = H;
+    a.D = D;
+    a.weight[0] = q_weight;
+    a.weight[1] = k_weight;
+    a.eps = eps;
+    a.cos = rope_cos;
+    a.sin = rope_sin;
+    a.out[0] = static_cast<uint16_t*>(q_out);
+    a.out[1] = static_cast<uint16_t*>(k_out);
+    a.out[2] = static_cast<uint16_t*>(v_out);
+    cudaError_t e = launch_qkv_norm_rope(a, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DIT_OK : DIT_ERR_CUDA;
 }
 

@@ -42,6 +42,16 @@
 //
 // Keys j >= kv_len are outside the K/V tensor maps (zero fill) and masked to
 // -inf in the last tile, so pad rows are never read.
+//
+// MASK variant: a general (B, T, T) mask -- one bit per (query, key), shared by
+// the heads -- also sets masked scores to -inf; rows i >= mask_rows attend every
+// valid key (the pad-row rule of "8 卡怎么分 token", "构造 padding mask").  Each
+// softmax thread loads its row's 128 mask bits per key tile with one 16-byte
+// load, issued a tile ahead.  A row whose keys are all masked so far has
+// m = -inf: its exponentials use 0 as the offset (all its P are 0), every
+// later tile takes the slow path until one sets a finite m (rescale factor 1
+// while m stays -inf), and a row with no allowed key at all ends with O = 0,
+// LSE = -inf.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -81,8 +91,8 @@ struct Cfg {
 };
 
 // ACCUM: fold this pass into an existing fp32 (O, LSE) pair instead of
-// overwriting it (streaming merge over key chunks).
-template <int D, bool OUT_BF16, bool ACCUM>
+// overwriting it (streaming merge over key chunks).  MASK: apply the bit mask.
+template <int D, bool OUT_BF16, bool ACCUM, bool MASK>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
@@ -267,6 +277,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m = -INFINITY;  // running max of scale*log2(e)*s (possibly stale)
         float l = 0.f;        // running sum of 2^(s*sl2 - m)
         bool ok = true;
+        // MASK: this row's bit words (all ones for rows past mask_rows)
+        const bool row_masked = MASK && row < a.mask_rows;
+        const uint32_t* mrow = MASK ? a.mask + static_cast<int64_t>(b) * a.mask_sb + static_cast<int64_t>(row_masked ? row : 0) * a.mask_si
+                                    : nullptr;
+        uint4 mw = make_uint4(~0u, ~0u, ~0u, ~0u);
+        if (MASK && row_masked && n_tiles > 0) mw = __ldg(reinterpret_cast<const uint4*>(mrow));
+        // offset used in the exponent: 0 while no key of the row has been seen
+        auto m_off = [&](float mm) { return (MASK && mm == -INFINITY) ? 0.f : mm; };
 
         // max over 64 scores: eight 3-input max chains, then a small tree.
         auto max64 = [](const float* v) {
@@ -318,6 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tS + 64, sr[2]);
             tmem_ld32(tS + 96, sr[3]);
             const int valid = a.kv_len - j * kBN;   // >= 1
+            uint4 mcur = mw;
+            if (MASK && row_masked && j + 1 < n_tiles) mw = __ldg(reinterpret_cast<const uint4*>(mrow) + (j + 1));
             float s[128];
 #pragma unroll
             for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
@@ -325,6 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
                     if (c >= valid) s[c] = -INFINITY;
+            }
+            if constexpr (MASK) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (!(((c < 32 ? mcur.x : mcur.y) >> (c & 31)) & 1u)) s[c] = -INFINITY;
             }
             if (j == 0) {
                 const float mxA = max64(s);
@@ -338,15 +363,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 64; c < 128; ++c)
                         if (c >= valid) s[c] = -INFINITY;
                 }
+                if constexpr (MASK) {
+#pragma unroll
+                    for (int c = 64; c < 128; ++c)
+                        if (!(((c < 96 ? mcur.z : mcur.w) >> (c & 31)) & 1u)) s[c] = -INFINITY;
+                }
                 m = fmaxf(mxA, max64(s + 64)) * sl2;
-                l = exp_store(s, tS, m) + exp_store(s + 64, tS + 32, m);
+                l = exp_store(s, tS, m_off(m)) + exp_store(s + 64, tS + 32, m_off(m));
             } else {
                 // Exponents with the running max m, no tile max: if the tile's row
                 // sum stays <= 2^39 then every P <= 2^39, which bf16 P and the fp32
                 // O / l accumulators hold exactly as well as P <= 1.  Rows whose sum
                 // exceeds it (their max grew by more than ~32 in log2 units) take
                 // the slow path: tile max, O rescale, P recomputed.
-                float lA = exp_store(s, tS, m);
+                float lA = exp_store(s, tS, m_off(m));
                 tmem_ld_wait_dep(sr[2]);
                 reg_dep(sr[3]);
 #pragma unroll
@@ -356,14 +386,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 64; c < 128; ++c)
                         if (c >= valid) s[c] = -INFINITY;
                 }
-                float lB = exp_store(s + 64, tS + 32, m);
-                const bool need = !(lA + lB <= kSumLimit);   // also true for inf / NaN
+                if constexpr (MASK) {
+#pragma unroll
+                    for (int c = 64; c < 128; ++c)
+                        if (!(((c < 96 ? mcur.z : mcur.w) >> (c & 31)) & 1u)) s[c] = -INFINITY;
+                }
+                float lB = exp_store(s + 64, tS + 32, m_off(m));
+                // also true for inf / NaN; MASK: a row with no key seen yet (m = -inf)
+                // always takes the slow path, which sets m from this tile's max
+                const bool need = !(lA + lB <= kSumLimit) || (MASK && m == -INFINITY);
                 if (__any_sync(0xffffffffu, need)) {
                     // O holds PV(j-1) already (S(j) was committed after it).
                     tmem_st_wait();
                     const float m_tile = fmaxf(max64(s), max64(s + 64)) * sl2;
                     const float m_new = need ? fmaxf(m_tile, m) : m;
-                    const float alpha = ex2_approx(m - m_new);
+                    const float alpha = (MASK && m_new == -INFINITY) ? 1.f : ex2_approx(m - m_new);
                     l *= alpha;
 #pragma unroll
                     for (int cc = 0; cc < D / 32; ++cc) {
@@ -375,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st32(tO + cc * 32, o);
                     }
                     m = m_new;
-                    lA = exp_store(s, tS, m);
-                    lB = exp_store(s + 64, tS + 32, m);
+                    lA = exp_store(s, tS, m_off(m));
+                    lB = exp_store(s + 64, tS + 32, m_off(m));
                 }
                 l += lA + lB;
             }
@@ -397,9 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t o_off = static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(row) * a.o_sn +
                                   static_cast<int64_t>(h) * a.o_sh;
             const int64_t lse_idx = (static_cast<int64_t>(b) * a.H + h) * a.Nq + row;
-            const float lse_new = n_tiles > 0 ? (m + log2f(l)) * kLn2 : -INFINITY;
+            const bool any_key = n_tiles > 0 && (!MASK || l > 0.f);
+            const float lse_new = any_key ? (m + log2f(l)) * kLn2 : -INFINITY;
             // out = c_prev * O_prev + c_new * O_tmem
-            float c_new = n_tiles > 0 ? 1.f / l : 0.f;
+            float c_new = any_key ? 1.f / l : 0.f;
             float c_prev = 0.f;
             float lse_out = lse_new;
             if constexpr (ACCUM) {
@@ -471,10 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool BF16, bool ACCUM>
+template <int D, bool BF16, bool ACCUM, bool MASK = false>
 cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& args,
                         int B, cudaStream_t stream) {
-    auto kern = attn_fwd_kernel<D, BF16, ACCUM>;
+    auto kern = attn_fwd_kernel<D, BF16, ACCUM, MASK>;
     const int smem = Cfg<D>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -487,6 +525,13 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const AttnArgs& args, int B, int D, bool out_bf16, bool accumulate, cudaStream_t stream) {
+    if (args.mask != nullptr) {
+        if (accumulate) return cudaErrorInvalidValue;
+        if (D == 128) return out_bf16 ? launch_impl<128, true, false, true>(tq, tk, tv, args, B, stream)
+                                      : launch_impl<128, false, false, true>(tq, tk, tv, args, B, stream);
+        return out_bf16 ? launch_impl<64, true, false, true>(tq, tk, tv, args, B, stream)
+                        : launch_impl<64, false, false, true>(tq, tk, tv, args, B, stream);
+    }
     if (accumulate) {
         if (out_bf16) return cudaErrorInvalidValue;
         return D == 128 ? launch_impl<128, false, true>(tq, tk, tv, args, B, stream)

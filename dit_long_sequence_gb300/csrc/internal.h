@@ -25,6 +25,9 @@ struct AttnArgs {
     int64_t o_sb, o_sn, o_sh;  // O element strides
     float* lse;        // [B, H, Nq]
     float o_scale;     // FP8 path: O multiplied by this (descale of V); unused by bf16
+    const uint32_t* mask;      // general mask bits (nullptr = none): bit j&31 of word
+    int64_t mask_sb, mask_si;  //   mask[b*mask_sb + i*mask_si + j/32], rows i < mask_rows
+    int mask_rows;
     unsigned int* status;      // device status word (4 x u32)
     unsigned long long timeout_ns;
 };
@@ -77,6 +80,19 @@ struct CastArgs {
 };
 
 cudaError_t launch_qkv_cast_fp8(const CastArgs& args, cudaStream_t stream);
+
+struct NormRopeArgs {
+    const uint16_t* qkv;        // bf16 [B, N, 3, H, D], (3, H, D) contiguous
+    int64_t stride_b, stride_n; // elements
+    int B, N, H, D;
+    const float* weight[2];     // RMSNorm weights [D] for q, k; nullptr = no norm for that tensor
+    float eps;
+    const float* cos;           // [N, D/2] fp32, nullptr = no rotation
+    const float* sin;
+    uint16_t* out[3];           // head-major [B, H, N, D]
+};
+
+cudaError_t launch_qkv_norm_rope(const NormRopeArgs& args, cudaStream_t stream);
 
 int device_sm_count(int device);
 

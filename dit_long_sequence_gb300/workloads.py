@@ -103,6 +103,45 @@ def randn_e4m3(shape, seed: int, scale: float, device="cpu") -> torch.Tensor:
     return x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
 
 
+def pack_mask_bits(mask, n_keys: int | None = None) -> torch.Tensor:
+    """Bit-pack a boolean [B, R, Nk] mask (True = may attend; torch or numpy)
+    into int32 words [B, R, W] on the host: bit (j & 31) of word j >> 5;
+    W = 4 * ceil(n_keys / 128) (whole 128-key tiles, zero bits past Nk).  Input
+    marshalling for the masked kernel."""
+    m = mask.cpu().numpy() if isinstance(mask, torch.Tensor) else np.asarray(mask)
+    B, R, Nk = m.shape
+    nk = Nk if n_keys is None else max(int(n_keys), Nk)
+    W = 4 * ((nk + 127) // 128)
+    out = np.zeros((B, R, W), dtype=np.uint32)
+    step = 4096
+    for r0 in range(0, R, step):
+        blk = np.zeros((B, min(step, R - r0), W * 32), dtype=bool)
+        blk[:, :, :Nk] = m[:, r0:r0 + step]
+        out[:, r0:r0 + step] = np.packbits(blk, axis=-1, bitorder="little").view("<u4")
+    return torch.from_numpy(out.view(np.int32))
+
+
+def rope_tables_3d(grid, D: int, base: float = 10000.0, device="cpu"):
+    """Rotary angle tables for a flattened (T, Hh, W) latent grid: the D/2
+    channel pairs are split over the three axes (1/4 time, 3/8 height, 3/8
+    width), pair i of an axis with d_a pairs turning at base^(-i/d_a) per grid
+    step.  Returns fp32 cos, sin [T*Hh*W, D/2] (angles formed in fp64).  An
+    input generator for the rotary step, shaped like a video DiT's 3-D RoPE."""
+    T, Hh, W = grid
+    half = D // 2
+    dt = half // 4
+    dh = (half - dt) // 2
+    dw = half - dt - dh
+    t, h, w = torch.meshgrid(torch.arange(T, dtype=torch.float64), torch.arange(Hh, dtype=torch.float64),
+                             torch.arange(W, dtype=torch.float64), indexing="ij")
+    parts = []
+    for pos, d in ((t, dt), (h, dh), (w, dw)):
+        freq = base ** (-torch.arange(d, dtype=torch.float64) / d)
+        parts.append(pos.reshape(-1, 1) * freq[None, :])
+    ang = torch.cat(parts, dim=1)
+    return ang.cos().to(torch.float32).to(device), ang.sin().to(torch.float32).to(device)
+
+
 def make_qkv(B: int, N: int, H: int, D: int, seed: int, device="cpu", fused: bool = False,
              Nkv: int | None = None):
     """Seeded bf16 q, k, v as [B, N, H, D] tensors.

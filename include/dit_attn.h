@@ -7,10 +7,13 @@
  *   dit_attn_fwd           softmax(scale * Q K^T) V plus the per-row
  *                          log-sum-exp, Q/K/V read through arbitrary
  *                          (b, n, h) strides, key-only padding mask.
+ *   dit_attn_fwd_masked    the same with a general (B, Nq, Nkv) bit mask.
  *   dit_attn_lse_merge     exact combine of (O, LSE) partials computed over
  *                          disjoint key chunks.
  *   dit_qkv_to_head_major  split of a fused [B, N, 3, H, D] projection
  *                          buffer into three head-major [B, H, N, D] tensors.
+ *   dit_qkv_norm_rope_to_head_major  the same split with Q/K RMSNorm and
+ *                          rotary embedding fused in (V copied).
  *   dit_qkv_cast_fp8       one-pass scaled bf16 -> E4M3 cast of that stacked
  *                          buffer, and dit_attn_fwd_fp8, the attention that
  *                          reads its output in place.
@@ -101,6 +104,40 @@ dit_status_t dit_attn_fwd(const void *q, const void *k, const void *v,
                           dit_stream_t stream);
 
 /*
+ * dit_attn_fwd_masked -- dit_attn_fwd with a general attention mask.
+ *
+ * Defined by "8 卡怎么分 token：LTX-2 序列并行的 all2all 到底搬了什么",
+ * "数据流拆解", paragraph "构造 padding mask": when the caller passes a
+ * (B, T, T) mask it is expanded over the pad rows and columns -- pad keys are
+ * masked and pad query rows may attend every valid key, since a row with every
+ * key masked would make a plain softmax NaN.  Cross-attention (Nq != Nkv, e.g.
+ * video queries over a short text or audio K/V) is the same call with any
+ * Nq, Nkv (and dit_attn_fwd without a mask).
+ *
+ * mask   device array of 32-bit words: query i may attend key j when bit (j & 31)
+ *        of mask[b*mask_batch_stride + i*mask_row_stride + (j >> 5)] is 1.  Read
+ *        only for rows i < mask_rows and keys j < key_valid_len; the mask is
+ *        shared by all heads.  Rows i >= mask_rows attend every key
+ *        j < key_valid_len (the pad-row rule); keys j >= key_valid_len are always
+ *        masked.  The kernel reads 4 * ceil(key_valid_len / 128) words of each
+ *        masked row, so mask_row_stride must be at least that; strides are
+ *        multiples of 4 words, mask_batch_stride >= 0 (0 shares one mask across
+ *        the batch), base 16-byte aligned, and the array must hold
+ *        (B-1)*mask_batch_stride + mask_rows*mask_row_stride words.
+ * mask_rows  0 <= mask_rows <= Nq; 0 makes the call dit_attn_fwd (mask unread).
+ * A row left with no allowed key gets O = 0 and LSE = -inf (weight 0 in a
+ * merge) instead of NaN.  Other arguments as dit_attn_fwd.
+ */
+dit_status_t dit_attn_fwd_masked(const void *q, const void *k, const void *v,
+                                 const dit_attn_strides_t *strides,
+                                 int B, int Nq, int Nkv, int H, int D,
+                                 int key_valid_len,
+                                 const uint32_t *mask, int64_t mask_batch_stride,
+                                 int64_t mask_row_stride, int mask_rows,
+                                 float scale, void *out, dit_dtype_t out_dtype, float *lse,
+                                 dit_stream_t stream);
+
+/*
  * dit_attn_fwd_accumulate -- one more key chunk folded into a running result.
  *
  * The streaming form of the merge: "Scaling Video Generation Across NVL72 rack
@@ -176,6 +213,37 @@ dit_status_t dit_qkv_to_head_major(const void *qkv, int64_t stride_b, int64_t st
                                    int B, int N, int H, int D,
                                    void *q_out, void *k_out, void *v_out,
                                    dit_stream_t stream);
+
+/*
+ * dit_qkv_norm_rope_to_head_major -- dit_qkv_to_head_major with the per-head
+ * normalisation and rotary embedding of Q and K fused into the same pass.
+ *
+ * Defined by "CUDA IPC Ulysses：在 H100 上重叠 Attention 通信", "基线与瓶颈"
+ * and "模型调度": after the fused QKV projection, Q and K get normalisation and
+ * RoPE, V does not.  The pages give neither formula; this call implements
+ * RMSNorm over the head dimension followed by the RoFormer rotation of
+ * consecutive channel pairs:
+ *   y_d = x_d / sqrt(mean_d(x_d^2) + eps) * w_d                (w = q_weight / k_weight)
+ *   (y_2i, y_2i+1) -> (y_2i c - y_2i+1 s, y_2i s + y_2i+1 c),  c = rope_cos[n*D/2 + i],
+ *                                                              s = rope_sin[n*D/2 + i],
+ * computed in fp32 and rounded to bf16 once.
+ *
+ * qkv, stride_b, stride_n, B, N, H, q_out, k_out, v_out  as dit_qkv_to_head_major.
+ * D          64 or 128.
+ * q_weight, k_weight  fp32 [D] device arrays, 16-byte aligned; NULL skips the
+ *            normalisation of that tensor.
+ * eps        finite, >= 0.
+ * rope_cos, rope_sin  fp32 [N, D/2] contiguous device arrays, 16-byte aligned,
+ *            one row per sequence position (any 1-D or multi-axis angle table);
+ *            both NULL skips the rotation, one NULL is DIT_ERR_INVALID_ARG.
+ * v_out receives V bit-exactly.
+ */
+dit_status_t dit_qkv_norm_rope_to_head_major(const void *qkv, int64_t stride_b, int64_t stride_n,
+                                             int B, int N, int H, int D,
+                                             const float *q_weight, const float *k_weight, float eps,
+                                             const float *rope_cos, const float *rope_sin,
+                                             void *q_out, void *k_out, void *v_out,
+                                             dit_stream_t stream);
 
 /*
  * dit_qkv_cast_fp8 -- one pass over a stacked bf16 QKV buffer that writes it

@@ -48,8 +48,8 @@ def compare(O_gpu: np.ndarray, L_gpu: np.ndarray, O_ref: np.ndarray, L_ref: np.n
             o_max=O_MAX_ABS, o_mean=O_MEAN_ABS, lse_max=LSE_MAX_ABS, rel_l2=O_REL_L2):
     """Element-wise gates; returns a dict of the measured errors."""
     dO = np.abs(O_gpu - O_ref)
-    dL = np.abs(L_gpu - L_ref)
     finite = np.isfinite(L_ref)
+    dL = np.where(finite, np.abs(np.where(finite, L_gpu, 0.0) - np.where(finite, L_ref, 0.0)), 0.0)
     res = {
         "o_max_abs": float(dO.max()) if dO.size else 0.0,
         "o_mean_abs": float(dO.mean()) if dO.size else 0.0,

@@ -170,3 +170,42 @@ def test_cast_fp8_argument_checks(lib):
     assert call(N=-1) == lib.DIT_ERR_INVALID_ARG
     assert call(B=4, N=1 << 20, H=64, D=128, sn=3 * 64 * 128) == lib.DIT_ERR_UNSUPPORTED   # >= 2^32 chunks
     assert call(N=0) == lib.DIT_OK
+
+
+def test_norm_rope_argument_checks(lib):
+    f = lib.raw().dit_qkv_norm_rope_to_head_major
+    ok = [FAKE, 0, 3 * 4 * 64, 1, 8, 4, 64, FAKE, FAKE, 1e-6, FAKE, FAKE + 4096, FAKE, FAKE, FAKE, None]
+    names = ["qkv", "sb", "sn", "B", "N", "H", "D", "wq", "wk", "eps", "cos", "sin", "q", "k", "v", "s"]
+
+    def call(**kw):
+        a = list(ok)
+        for k_, v_ in kw.items():
+            a[names.index(k_)] = v_
+        return f(*a)
+    assert call(D=32, sn=3 * 4 * 32) == lib.DIT_ERR_UNSUPPORTED
+    assert call(eps=-1.0) == lib.DIT_ERR_INVALID_ARG
+    assert call(eps=float("nan")) == lib.DIT_ERR_INVALID_ARG
+    assert call(sin=None) == lib.DIT_ERR_INVALID_ARG            # one table without the other
+    assert call(wq=FAKE + 4) == lib.DIT_ERR_ALIGNMENT
+    assert call(cos=FAKE + 8) == lib.DIT_ERR_ALIGNMENT
+    assert call(sn=3 * 4 * 64 + 4) == lib.DIT_ERR_ALIGNMENT
+    assert call(v=None) == lib.DIT_ERR_INVALID_ARG
+    assert call(N=0) == lib.DIT_OK
+
+
+def test_masked_argument_checks(lib):
+    st = lib.AttnStrides(*(lib.Strides4(8 * 128 * 4, 4 * 128, 128, 1) for _ in range(4)))
+    f = lib.raw().dit_attn_fwd_masked
+
+    def call(mask=FAKE, sb=0, si=4, rows=8, kvl=8, B=1):
+        return f(FAKE, FAKE, FAKE, ctypes.byref(st), B, 8, 8, 4, 128, kvl, mask, sb, si, rows, 0.088, FAKE,
+                 lib.DIT_F32, FAKE, None)
+    assert call(rows=9) == lib.DIT_ERR_INVALID_ARG          # more mask rows than queries
+    assert call(rows=-1) == lib.DIT_ERR_INVALID_ARG
+    assert call(mask=None) == lib.DIT_ERR_INVALID_ARG
+    assert call(si=2) == lib.DIT_ERR_INVALID_ARG             # fewer words than one key tile reads
+    assert call(si=6) == lib.DIT_ERR_ALIGNMENT
+    assert call(sb=2) == lib.DIT_ERR_ALIGNMENT
+    assert call(mask=FAKE + 4) == lib.DIT_ERR_ALIGNMENT
+    assert call(sb=-4) == lib.DIT_ERR_INVALID_ARG
+    assert call(B=0) == lib.DIT_OK
