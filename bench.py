@@ -367,6 +367,48 @@ def time_norm_rope_kernel(step, reps=5):
     return 2 * step.inputs[0].numel() * 2, statistics.median(ts)
 
 
+def time_masked_attention(step, reps=3):
+    """The general-mask variant (dit_attn_fwd_masked) on the step's q/k/v with
+    a (T, T) user mask over the valid tokens -- frame-local blocks of 1,512
+    tokens plus ~5% hashed long-range links -- against the unmasked kernel;
+    FLOPs counted as for the unmasked path (every score is computed)."""
+    import numpy as np
+    import torch
+    from dit_long_sequence_gb300 import workloads as wl
+    w = step.w
+    T = w.kv_len
+    words = np.zeros((1, T, 4 * ((T + 127) // 128)), dtype=np.int32)
+    cols = np.arange(T, dtype=np.int64)
+    for r0 in range(0, T, 2048):
+        r = np.arange(r0, min(T, r0 + 2048), dtype=np.int64)[:, None]
+        m = ((r // 1512) == (cols[None, :] // 1512)) | (((r * 1103515245 + cols[None, :] * 12345 + 7) >> 9) % 20 == 0)
+        words[0, r0:r0 + m.shape[0]] = wl.pack_mask_bits(m[None]).numpy()[0]
+    bits = torch.from_numpy(words).to(step.dev)
+    q, k, v = step.q, step.k, step.v
+    s = step.stream
+    out = {}
+    for name, fn in (("masked", lambda: step.dl.attn_fwd_masked(q, k, v, bits, key_valid_len=T, out=step.out,
+                                                                   lse=step.lse, stream=s)),
+                     ("unmasked", lambda: step.dl.attn_fwd(q, k, v, key_valid_len=T, out=step.out, lse=step.lse,
+                                                           stream=s))):
+        fn()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        out[name] = {"ms": ms, "TFLOP/s": w.flops() / (ms * 1e-3) / 1e12}
+    density = float(np.unpackbits(words[0, :2048].view(np.uint8), bitorder="little").mean()) * \
+        (words.shape[2] * 32) / T
+    out["mask_density"] = density
+    del bits
+    return out
+
+
 # --------------------------------------------------------------- cpu baseline
 
 def cpu_baseline(w, dev_inputs=None, target_s=12.0):
@@ -487,6 +529,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--masked", action="store_true",
+                    help="also time the general-mask attention variant on this workload (bf16 workloads)")
     args = ap.parse_args(argv)
     from dit_long_sequence_gb300 import workloads as wl
     w = wl.WORKLOADS[args.workload]
@@ -565,6 +609,9 @@ def main(argv=None):
         mb, mms = time_merge_kernel(dev, w.B, w.N, w.H, w.D, n_chunks=9, interleaved=il)
         mgbs = mb / (mms * 1e-3) / 1e9
         extra[key] = {"bytes": mb, "ms": mms, "GB/s": mgbs, "frac_hbm": mgbs / float(peaks["hbm_gbs"])}
+
+    if args.masked and not w.fp8:
+        extra["attn_masked"] = time_masked_attention(step)
 
     # ---------------- end-to-end through host buffers
     e2e = None
