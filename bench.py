@@ -369,9 +369,11 @@ def time_norm_rope_kernel(step, reps=5):
 
 def time_masked_attention(step, reps=3):
     """The general-mask variant (dit_attn_fwd_masked) on the step's q/k/v with
-    a (T, T) user mask over the valid tokens -- frame-local blocks of 1,512
-    tokens plus ~5% hashed long-range links -- against the unmasked kernel;
-    FLOPs counted as for the unmasked path (every score is computed)."""
+    (T, T) user masks over the valid tokens -- frame-local blocks of 1,512
+    tokens plus ~5% hashed long-range links (no empty key tile), and the
+    frame-local blocks alone (most key tiles empty: with and without the
+    occupancy workspace) -- against the unmasked kernel.  TFLOP/s counts the
+    unmasked FLOPs, i.e. it is an equivalent rate."""
     import numpy as np
     import torch
     from dit_long_sequence_gb300 import workloads as wl
@@ -384,11 +386,23 @@ def time_masked_attention(step, reps=3):
         m = ((r // 1512) == (cols[None, :] // 1512)) | (((r * 1103515245 + cols[None, :] * 12345 + 7) >> 9) % 20 == 0)
         words[0, r0:r0 + m.shape[0]] = wl.pack_mask_bits(m[None]).numpy()[0]
     bits = torch.from_numpy(words).to(step.dev)
+    # frame-local blocks only (no long-range links): most key tiles are empty
+    local = np.zeros_like(words)
+    for r0 in range(0, T, 2048):
+        r = np.arange(r0, min(T, r0 + 2048), dtype=np.int64)[:, None]
+        local[0, r0:r0 + r.shape[0]] = wl.pack_mask_bits(((r // 1512) == (cols[None, :] // 1512))[None]).numpy()[0]
+    local_bits = torch.from_numpy(local).to(step.dev)
+    ws = torch.empty(max(16, step.dl.masked_workspace_bytes(w.B, w.N, T)), dtype=torch.uint8, device=step.dev)
     q, k, v = step.q, step.k, step.v
     s = step.stream
     out = {}
     for name, fn in (("masked", lambda: step.dl.attn_fwd_masked(q, k, v, bits, key_valid_len=T, out=step.out,
-                                                                   lse=step.lse, stream=s)),
+                                                                   lse=step.lse, workspace=ws, stream=s)),
+                     ("masked_frame_local_skip", lambda: step.dl.attn_fwd_masked(
+                         q, k, v, local_bits, key_valid_len=T, out=step.out, lse=step.lse, workspace=ws, stream=s)),
+                     ("masked_frame_local_no_skip", lambda: step.dl.attn_fwd_masked(
+                         q, k, v, local_bits, key_valid_len=T, out=step.out, lse=step.lse,
+                         skip_empty_tiles=False, stream=s)),
                      ("unmasked", lambda: step.dl.attn_fwd(q, k, v, key_valid_len=T, out=step.out, lse=step.lse,
                                                            stream=s))):
         fn()

@@ -46,7 +46,9 @@ _lib.dit_attn_fwd_accumulate.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrid
                                          _vp, _vp, _vp]
 _lib.dit_attn_fwd_masked.restype = _i
 _lib.dit_attn_fwd_masked.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _vp, _i64,
-                                     _i64, _i, _f, _vp, _i, _vp, _vp]
+                                     _i64, _i, _f, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]
+_lib.dit_attn_masked_workspace_bytes.restype = ctypes.c_size_t
+_lib.dit_attn_masked_workspace_bytes.argtypes = [_i, _i, _i]
 _lib.dit_attn_fwd_fp8.restype = _i
 _lib.dit_attn_fwd_fp8.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f, _f, _f, _f,
                                   _vp, _i, _vp, _vp]
@@ -67,7 +69,7 @@ _lib.dit_check_watchdog.restype = _i
 _lib.dit_check_watchdog.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
 _lib.dit_version.restype = ctypes.c_uint32
 
-EXPORTS = ("dit_attn_fwd", "dit_attn_fwd_masked", "dit_attn_fwd_accumulate", "dit_attn_lse_merge", "dit_qkv_to_head_major",
+EXPORTS = ("dit_attn_fwd", "dit_attn_fwd_masked", "dit_attn_masked_workspace_bytes", "dit_attn_fwd_accumulate", "dit_attn_lse_merge", "dit_qkv_to_head_major",
            "dit_qkv_norm_rope_to_head_major", "dit_qkv_cast_fp8", "dit_attn_fwd_fp8", "dit_status_string",
            "dit_check_watchdog",
            "dit_watchdog_selftest", "dit_version")
@@ -132,16 +134,24 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, key_valid_len
     return out, lse
 
 
+def masked_workspace_bytes(B: int, Nq: int, key_valid_len: int) -> int:
+    """Workspace that lets attn_fwd_masked skip key tiles the mask leaves empty."""
+    return int(_lib.dit_attn_masked_workspace_bytes(int(B), int(Nq), int(key_valid_len)))
+
+
 def attn_fwd_masked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_bits: torch.Tensor, *,
                     mask_rows: int | None = None, key_valid_len: int | None = None, scale: float | None = None,
                     out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-                    out_dtype: torch.dtype = torch.float32, stream=None):
+                    out_dtype: torch.dtype = torch.float32, workspace: torch.Tensor | None = None,
+                    skip_empty_tiles: bool = True, stream=None):
     """Attention with a general bit mask through `dit_attn_fwd_masked`.
 
     mask_bits: int32 CUDA tensor [B or 1, R, W] of packed bits (bit j&31 of word
     j>>5 of row i: query i may attend key j), W a multiple of 4 with
     W >= 4*ceil(key_valid_len/128); a leading dimension of 1 shares the mask
     across the batch.  Rows i >= mask_rows (default R) attend every valid key.
+    With skip_empty_tiles (default) a workspace (allocated here unless given)
+    lets the kernel skip key tiles the mask leaves empty.
     """
     B, Nq, H, D = q.shape
     Nkv = k.shape[1]
@@ -168,11 +178,18 @@ def attn_fwd_masked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_bits
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
     sb = 0 if mask_bits.shape[0] == 1 else mask_bits.stride(0)
+    ws_ptr, ws_bytes = None, 0
+    if skip_empty_tiles:
+        need = masked_workspace_bytes(B, Nq, kvl)
+        if workspace is None and need > 0:
+            workspace = torch.empty((need + 15) // 16 * 16, dtype=torch.uint8, device=q.device)
+        if workspace is not None:
+            ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     st = AttnStrides(_strides4(q), _strides4(k), _strides4(v), _strides4(out))
     rc = _lib.dit_attn_fwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(st), B, Nq, Nkv, H, D, kvl,
                                   mask_bits.data_ptr(), sb, mask_bits.stride(1), rows, sc, out.data_ptr(),
                                   DIT_F32 if out.dtype == torch.float32 else DIT_BF16, lse.data_ptr(),
-                                  _stream_ptr(stream))
+                                  ws_ptr, ws_bytes, _stream_ptr(stream))
     _check(rc, "dit_attn_fwd_masked")
     return out, lse
 

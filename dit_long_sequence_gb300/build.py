@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libditattn.so")
 SOURCES = ["api.cu", "attn_fwd.cu", "attn_fwd_fp8.cu", "qkv_cast_fp8.cu", "lse_merge.cu", "qkv_layout.cu",
-           "qkv_norm_rope.cu", "selftest.cu"]
+           "qkv_norm_rope.cu", "mask_occupancy.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

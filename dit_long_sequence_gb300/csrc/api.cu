@@ -121,7 +121,13 @@ struct MaskSpec {
     const uint32_t* bits;
     int64_t batch_stride, row_stride;   // in 32-bit words
     int rows;
+    uint32_t* occ;                      // occupancy map (workspace) or nullptr
 };
+
+int64_t occ_words_of(int key_valid_len) { return ((key_valid_len + 127) / 128 + 31) / 32; }
+int64_t occ_bytes_of(int B, int Nq, int key_valid_len) {
+    return static_cast<int64_t>(B) * ((Nq + 255) / 256) * occ_words_of(key_valid_len) * 4;
+}
 
 // fp8: E4M3 inputs (D = 128 only), descales[3] = (q, k, v); otherwise bf16.
 // mask: the general bit mask of dit_attn_fwd_masked (bf16 only).
@@ -176,6 +182,9 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DIT_ERR_CUDA;
     AttnArgs a;
+    a.status = status_word(dev);
+    a.timeout_ns = kWatchdogNs;
+    if (a.status == nullptr) return DIT_ERR_CUDA;   // checked before anything is enqueued
     a.Nq = Nq;
     a.H = H;
     a.kv_len = key_valid_len;
@@ -185,20 +194,37 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
     a.mask = nullptr;
     a.mask_sb = a.mask_si = 0;
     a.mask_rows = 0;
+    a.occ = nullptr;
+    a.occ_words = 0;
     if (mask != nullptr && mask->rows > 0 && any_keys) {
         a.mask = mask->bits;
         a.mask_sb = mask->batch_stride;
         a.mask_si = mask->row_stride;
         a.mask_rows = mask->rows;
+        if (mask->occ != nullptr) {
+            OccArgs o;
+            o.mask = mask->bits;
+            o.mask_sb = mask->batch_stride;
+            o.mask_si = mask->row_stride;
+            o.mask_rows = mask->rows;
+            o.B = B;
+            o.Nq = Nq;
+            o.kv_len = key_valid_len;
+            o.n_kv_tiles = a.n_kv_tiles;
+            o.row_blocks = (Nq + 255) / 256;
+            o.occ_words = static_cast<int>(occ_words_of(key_valid_len));
+            o.occ = mask->occ;
+            cudaError_t e = launch_mask_occupancy(o, reinterpret_cast<cudaStream_t>(stream));
+            if (e != cudaSuccess) return DIT_ERR_CUDA;
+            a.occ = mask->occ;
+            a.occ_words = o.occ_words;
+        }
     }
     a.out = out;
     a.o_sb = so.b;
     a.o_sn = so.n;
     a.o_sh = so.h;
     a.lse = lse;
-    a.status = status_word(dev);
-    a.timeout_ns = kWatchdogNs;
-    if (a.status == nullptr) return DIT_ERR_CUDA;
     cudaError_t e = fp8 ? launch_attn_fwd_fp8(tq, tk, tv, a, B, out_dtype == DIT_BF16,
                                               reinterpret_cast<cudaStream_t>(stream))
                         : launch_attn_fwd(tq, tk, tv, a, B, D, out_dtype == DIT_BF16, accumulate,
@@ -224,18 +250,30 @@ dit_status_t dit_attn_fwd_accumulate(const void* q, const void* k, const void* v
                            stream);
 }
 
+size_t dit_attn_masked_workspace_bytes(int B, int Nq, int key_valid_len) {
+    if (B <= 0 || Nq <= 0 || key_valid_len <= 0) return 0;
+    return static_cast<size_t>(occ_bytes_of(B, Nq, key_valid_len));
+}
+
 dit_status_t dit_attn_fwd_masked(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides,
                                  int B, int Nq, int Nkv, int H, int D, int key_valid_len, const uint32_t* mask,
                                  int64_t mask_batch_stride, int64_t mask_row_stride, int mask_rows, float scale,
-                                 void* out, dit_dtype_t out_dtype, float* lse, dit_stream_t stream) {
+                                 void* out, dit_dtype_t out_dtype, float* lse, void* workspace,
+                                 size_t workspace_bytes, dit_stream_t stream) {
     if (mask_rows < 0 || mask_rows > Nq) return DIT_ERR_INVALID_ARG;
+    if (workspace != nullptr) {
+        if (B > 0 && Nq > 0 && key_valid_len > 0 &&
+            workspace_bytes < static_cast<size_t>(occ_bytes_of(B, Nq, key_valid_len)))
+            return DIT_ERR_INVALID_ARG;
+        if (!aligned16(workspace)) return DIT_ERR_ALIGNMENT;
+    }
     if (mask_rows > 0) {
         if (mask == nullptr) return DIT_ERR_INVALID_ARG;
         const int64_t words_read = 4 * static_cast<int64_t>((key_valid_len + 127) / 128);
         if (mask_row_stride < words_read || mask_batch_stride < 0) return DIT_ERR_INVALID_ARG;
         if (mask_row_stride % 4 || mask_batch_stride % 4 || !aligned16(mask)) return DIT_ERR_ALIGNMENT;
     }
-    const MaskSpec spec{mask, mask_batch_stride, mask_row_stride, mask_rows};
+    const MaskSpec spec{mask, mask_batch_stride, mask_row_stride, mask_rows, static_cast<uint32_t*>(workspace)};
     return attn_fwd_common(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, scale, out, out_dtype, lse, false,
                            stream, nullptr, &spec);
 }

@@ -51,7 +51,10 @@
 // m = -inf: its exponentials use 0 as the offset (all its P are 0), every
 // later tile takes the slow path until one sets a finite m (rescale factor 1
 // while m stays -inf), and a row with no allowed key at all ends with O = 0,
-// LSE = -inf.
+// LSE = -inf.  With an occupancy map (one bit per (256-row block, key tile):
+// does any row of the block attend any key of the tile), every role walks only
+// the occupied key tiles -- the TMA producer loads, the MMA thread multiplies
+// and the softmax warps exponentiate nothing else.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -60,6 +63,35 @@
 
 namespace dit {
 namespace {
+
+// Walks the set bits of one CTA's occupancy words (the key tiles to process);
+// without a map every tile is occupied.
+struct TileCursor {
+    const uint32_t* words;   // nullptr: all n tiles
+    int n_words, n, w;
+    uint32_t bits;
+    int next_all;
+    __device__ TileCursor(const uint32_t* occ, int n_tiles)
+        : words(occ), n_words((n_tiles + 31) / 32), n(n_tiles), w(0), bits(occ ? occ[0] : 0u), next_all(0) {}
+    // The next key tile to process, or -1.
+    __device__ int next() {
+        if (words == nullptr) return next_all < n ? next_all++ : -1;
+        while (bits == 0u) {
+            if (++w >= n_words) return -1;
+            bits = words[w];
+        }
+        const int t = w * 32 + __ffs(static_cast<int>(bits)) - 1;
+        bits &= bits - 1u;
+        return t < n ? t : -1;
+    }
+};
+
+__device__ __forceinline__ int count_tiles(const uint32_t* occ, int n_tiles) {
+    if (occ == nullptr) return n_tiles;
+    int c = 0;
+    for (int w = 0; w < (n_tiles + 31) / 32; ++w) c += __popc(occ[w]);
+    return c;
+}
 
 constexpr int kBM = 128;           // query rows per tile
 constexpr int kBN = 128;           // keys per KV tile
@@ -116,7 +148,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = blockIdx.y;
     const int b = blockIdx.z;
     const int q_row0 = blockIdx.x * (2 * kBM);
-    const int n_tiles = a.n_kv_tiles;
+    // MASK with an occupancy map: this CTA's row of tile bits
+    const uint32_t* occ = (MASK && a.occ != nullptr)
+                              ? a.occ + (static_cast<int64_t>(b) * gridDim.x + blockIdx.x) * a.occ_words
+                              : nullptr;
+    const int n_tiles = count_tiles(occ, a.n_kv_tiles);   // key tiles this CTA processes
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::kQFull + 0), 1);
@@ -166,7 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int total = 2 * n_tiles;
             int issued = 0;
+            TileCursor cur(occ, a.n_kv_tiles);
+            int key0 = 0;
             for (int i = 0; i < total; ++i) {
+                if ((i & 1) == 0) key0 = cur.next() * kBN;
                 const int slot = i % S;
                 const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
                 if (!wait_bounded(bar(C::kKVEmpty + slot), ph ^ 1u, wd, ROLE_LOAD, SITE_KV_EMPTY)) break;
@@ -174,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const CUtensorMap* tm = (i & 1) ? &tm_v : &tm_k;
                 const uint32_t dst = sRing + slot * TILE;
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d(dst + c * C::kBlockBytes, tm, bar(C::kKVFull + slot), c * 64, (i >> 1) * kBN, h, b);
+                    tma_load_4d(dst + c * C::kBlockBytes, tm, bar(C::kKVFull + slot), c * 64, key0, h, b);
                 issued = i + 1;
             }
             if (issued < total || *abort_flag) {
@@ -281,8 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_masked = MASK && row < a.mask_rows;
         const uint32_t* mrow = MASK ? a.mask + static_cast<int64_t>(b) * a.mask_sb + static_cast<int64_t>(row_masked ? row : 0) * a.mask_si
                                     : nullptr;
+        TileCursor cur(occ, a.n_kv_tiles);
+        int tile_next = n_tiles > 0 ? cur.next() : -1;   // key tile of the next iteration
         uint4 mw = make_uint4(~0u, ~0u, ~0u, ~0u);
-        if (MASK && row_masked && n_tiles > 0) mw = __ldg(reinterpret_cast<const uint4*>(mrow));
+        if (MASK && row_masked && n_tiles > 0) mw = __ldg(reinterpret_cast<const uint4*>(mrow) + tile_next);
         // offset used in the exponent: 0 while no key of the row has been seen
         auto m_off = [&](float mm) { return (MASK && mm == -INFINITY) ? 0.f : mm; };
 
@@ -335,9 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             reg_dep(sr[1]);
             tmem_ld32(tS + 64, sr[2]);
             tmem_ld32(tS + 96, sr[3]);
-            const int valid = a.kv_len - j * kBN;   // >= 1
+            const int tile = tile_next;
+            tile_next = j + 1 < n_tiles ? cur.next() : -1;
+            const int valid = a.kv_len - tile * kBN;   // >= 1
             uint4 mcur = mw;
-            if (MASK && row_masked && j + 1 < n_tiles) mw = __ldg(reinterpret_cast<const uint4*>(mrow) + (j + 1));
+            if (MASK && row_masked && j + 1 < n_tiles) mw = __ldg(reinterpret_cast<const uint4*>(mrow) + tile_next);
             float s[128];
 #pragma unroll
             for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);

@@ -28,6 +28,8 @@ struct AttnArgs {
     const uint32_t* mask;      // general mask bits (nullptr = none): bit j&31 of word
     int64_t mask_sb, mask_si;  //   mask[b*mask_sb + i*mask_si + j/32], rows i < mask_rows
     int mask_rows;
+    const uint32_t* occ;       // MASK: occupancy bits per (b, 256-row block), occ_words each; nullptr = all tiles
+    int occ_words;
     unsigned int* status;      // device status word (4 x u32)
     unsigned long long timeout_ns;
 };
@@ -93,6 +95,18 @@ struct NormRopeArgs {
 };
 
 cudaError_t launch_qkv_norm_rope(const NormRopeArgs& args, cudaStream_t stream);
+
+// Occupancy pre-pass of the masked attention: bit t of occ[(b*RB + rb)*occ_words + t/32]
+// is set when any row of the 256-row block rb attends any key of key tile t.
+struct OccArgs {
+    const uint32_t* mask;       // bit words, as AttnArgs
+    int64_t mask_sb, mask_si;
+    int mask_rows;
+    int B, Nq, kv_len, n_kv_tiles, row_blocks, occ_words;
+    uint32_t* occ;
+};
+
+cudaError_t launch_mask_occupancy(const OccArgs& args, cudaStream_t stream);
 
 int device_sm_count(int device);
 

@@ -38,6 +38,7 @@
 #ifndef DIT_ATTN_H
 #define DIT_ATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -126,7 +127,14 @@ dit_status_t dit_attn_fwd(const void *q, const void *k, const void *v,
  *        (B-1)*mask_batch_stride + mask_rows*mask_row_stride words.
  * mask_rows  0 <= mask_rows <= Nq; 0 makes the call dit_attn_fwd (mask unread).
  * A row left with no allowed key gets O = 0 and LSE = -inf (weight 0 in a
- * merge) instead of NaN.  Other arguments as dit_attn_fwd.
+ * merge) instead of NaN.
+ * workspace  NULL, or device memory of at least dit_attn_masked_workspace_bytes
+ *        (16-byte aligned) owned by the caller and not used by anything else
+ *        until the stream has passed the call: a pre-pass records which
+ *        128-key tiles each 256-row query block attends at all, and the
+ *        attention then loads and multiplies only those (block-local masks
+ *        skip most tiles).  NULL processes every tile (same results).
+ * Other arguments as dit_attn_fwd.
  */
 dit_status_t dit_attn_fwd_masked(const void *q, const void *k, const void *v,
                                  const dit_attn_strides_t *strides,
@@ -135,7 +143,16 @@ dit_status_t dit_attn_fwd_masked(const void *q, const void *k, const void *v,
                                  const uint32_t *mask, int64_t mask_batch_stride,
                                  int64_t mask_row_stride, int mask_rows,
                                  float scale, void *out, dit_dtype_t out_dtype, float *lse,
+                                 void *workspace, size_t workspace_bytes,
                                  dit_stream_t stream);
+
+/*
+ * dit_attn_masked_workspace_bytes -- bytes of `workspace` that let
+ * dit_attn_fwd_masked skip key tiles the mask leaves empty: one bit per
+ * (batch, 256-row query block, 128-key tile), written by a pre-pass on the
+ * same stream.  0 when there is nothing to compute.  Host only, no CUDA call.
+ */
+size_t dit_attn_masked_workspace_bytes(int B, int Nq, int key_valid_len);
 
 /*
  * dit_attn_fwd_accumulate -- one more key chunk folded into a running result.

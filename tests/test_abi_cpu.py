@@ -197,9 +197,9 @@ def test_masked_argument_checks(lib):
     st = lib.AttnStrides(*(lib.Strides4(8 * 128 * 4, 4 * 128, 128, 1) for _ in range(4)))
     f = lib.raw().dit_attn_fwd_masked
 
-    def call(mask=FAKE, sb=0, si=4, rows=8, kvl=8, B=1):
+    def call(mask=FAKE, sb=0, si=4, rows=8, kvl=8, B=1, ws=None, wsb=0):
         return f(FAKE, FAKE, FAKE, ctypes.byref(st), B, 8, 8, 4, 128, kvl, mask, sb, si, rows, 0.088, FAKE,
-                 lib.DIT_F32, FAKE, None)
+                 lib.DIT_F32, FAKE, ws, wsb, None)
     assert call(rows=9) == lib.DIT_ERR_INVALID_ARG          # more mask rows than queries
     assert call(rows=-1) == lib.DIT_ERR_INVALID_ARG
     assert call(mask=None) == lib.DIT_ERR_INVALID_ARG
@@ -208,4 +208,9 @@ def test_masked_argument_checks(lib):
     assert call(sb=2) == lib.DIT_ERR_ALIGNMENT
     assert call(mask=FAKE + 4) == lib.DIT_ERR_ALIGNMENT
     assert call(sb=-4) == lib.DIT_ERR_INVALID_ARG
+    assert call(ws=FAKE, wsb=2) == lib.DIT_ERR_INVALID_ARG     # smaller than the occupancy map
+    assert call(ws=FAKE + 4, wsb=4096) == lib.DIT_ERR_ALIGNMENT
     assert call(B=0) == lib.DIT_OK
+    ws = lib.raw().dit_attn_masked_workspace_bytes
+    assert ws(1, 24576, 24200) == 96 * 6 * 4                   # 96 row blocks x 190 tiles -> 6 words
+    assert ws(2, 256, 128) == 8 and ws(0, 10, 10) == 0 and ws(1, 10, 0) == 0

@@ -134,3 +134,40 @@ def test_masked_ltx_sized_sampled_rows(dl):
     allow[0, sel[sel >= T]] = True
     Or, Lr = oracle.attn(host_bits(q), host_bits(k), host_bits(v), key_valid_len=T, allow=allow, rows=rows)
     compare(*gather_rows(O, L, rows), Or, Lr)
+
+
+@pytest.mark.parametrize("skip", [True, False])
+def test_block_local_mask_skips_empty_tiles(dl, skip):
+    """Frame-local blocks: most (256-row block, 128-key tile) pairs are empty and,
+    with the workspace, skipped; a whole 256-row block with no allowed key
+    (a CTA with nothing to do) ends with O = 0, LSE = -inf; pad rows past
+    mask_rows attend every valid key.  Same results with and without skipping."""
+    B, T, Tp, H, D = 2, 3000, 3072, 2, 128
+    q, k, v, _ = wl.make_qkv(B, Tp, H, D, seed=41, device=DEV)
+    idx = torch.arange(T)
+    m = (idx[:, None] // 400) == (idx[None, :] // 400)
+    m = m[None].repeat(B, 1, 1)
+    m[1, 512:768] = False                      # one whole query block attends nothing
+    bits = wl.pack_mask_bits(m).to(DEV)
+    O, L = dl.attn_fwd_masked(q, k, v, bits, key_valid_len=T, skip_empty_tiles=skip)
+    torch.cuda.synchronize()
+    Or, Lr = oracle.attn(host_bits(q), host_bits(k), host_bits(v), key_valid_len=T,
+                         allow=oracle.expand_mask(m.numpy(), Tp))
+    compare(*_full(O, L), Or.transpose(0, 2, 1, 3), Lr)
+    assert torch.all(O[1, 512:768] == 0) and torch.all(torch.isneginf(L[1, :, 512:768]))
+
+
+def test_skipping_matches_full_walk_on_random_sparse_mask(dl):
+    B, T, H, D = 1, 2048, 2, 64
+    q, k, v, _ = wl.make_qkv(B, T, H, D, seed=43, device=DEV)
+    g = torch.Generator().manual_seed(43)
+    # sparse blocks of 128 x 128 kept at random, others empty
+    keep = torch.rand((T // 128, T // 128), generator=g) < 0.2
+    m = keep.repeat_interleave(128, 0).repeat_interleave(128, 1)[None]
+    bits = wl.pack_mask_bits(m).to(DEV)
+    O1, L1 = dl.attn_fwd_masked(q, k, v, bits, skip_empty_tiles=True)
+    O0, L0 = dl.attn_fwd_masked(q, k, v, bits, skip_empty_tiles=False)
+    torch.cuda.synchronize()
+    Or, Lr = oracle.attn(host_bits(q), host_bits(k), host_bits(v), allow=m.numpy())
+    compare(*_full(O1, L1), Or.transpose(0, 2, 1, 3), Lr)
+    compare(*_full(O0, L0), Or.transpose(0, 2, 1, 3), Lr)
