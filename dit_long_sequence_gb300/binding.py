@@ -47,6 +47,9 @@ _lib.dit_attn_fwd_accumulate.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrid
 _lib.dit_attn_fwd_masked.restype = _i
 _lib.dit_attn_fwd_masked.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _vp, _i64,
                                      _i64, _i, _f, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]
+_lib.dit_attn_fwd_masked_noalloc.restype = _i
+_lib.dit_attn_fwd_masked_noalloc.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _vp,
+                                             _i64, _i64, _i, _f, _vp, _i, _vp, _vp]
 _lib.dit_attn_masked_workspace_bytes.restype = ctypes.c_size_t
 _lib.dit_attn_masked_workspace_bytes.argtypes = [_i, _i, _i]
 _lib.dit_attn_fwd_fp8.restype = _i
@@ -69,7 +72,8 @@ _lib.dit_check_watchdog.restype = _i
 _lib.dit_check_watchdog.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
 _lib.dit_version.restype = ctypes.c_uint32
 
-EXPORTS = ("dit_attn_fwd", "dit_attn_fwd_masked", "dit_attn_masked_workspace_bytes", "dit_attn_fwd_accumulate", "dit_attn_lse_merge", "dit_qkv_to_head_major",
+EXPORTS = ("dit_attn_fwd", "dit_attn_fwd_masked", "dit_attn_fwd_masked_noalloc", "dit_attn_masked_workspace_bytes",
+           "dit_attn_fwd_accumulate", "dit_attn_lse_merge", "dit_qkv_to_head_major",
            "dit_qkv_norm_rope_to_head_major", "dit_qkv_cast_fp8", "dit_attn_fwd_fp8", "dit_status_string",
            "dit_check_watchdog",
            "dit_watchdog_selftest", "dit_version")
@@ -191,6 +195,38 @@ def attn_fwd_masked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_bits
                                   DIT_F32 if out.dtype == torch.float32 else DIT_BF16, lse.data_ptr(),
                                   ws_ptr, ws_bytes, _stream_ptr(stream))
     _check(rc, "dit_attn_fwd_masked")
+    return out, lse
+
+
+def attn_fwd_masked_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_bits: torch.Tensor, *,
+                            mask_rows: int | None = None, key_valid_len: int | None = None,
+                            scale: float | None = None, out: torch.Tensor | None = None,
+                            lse: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32, stream=None):
+    """attn_fwd_masked through `dit_attn_fwd_masked_noalloc`: the tile-occupancy
+    scratch is the library's fixed per-device array, no workspace is passed.
+    out and lse must be given (or are allocated here by PyTorch, not by the
+    library)."""
+    B, Nq, H, D = q.shape
+    Nkv = k.shape[1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a bf16 CUDA tensor")
+    if mask_bits.dtype != torch.int32 or mask_bits.dim() != 3 or mask_bits.stride(2) != 1 or not mask_bits.is_cuda:
+        raise ValueError("mask_bits must be an int32 CUDA tensor [B or 1, rows, words], words contiguous")
+    rows = mask_bits.shape[1] if mask_rows is None else int(mask_rows)
+    kvl = Nkv if key_valid_len is None else int(key_valid_len)
+    sc = float(D) ** -0.5 if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, Nq, H, D), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    sb = 0 if mask_bits.shape[0] == 1 else mask_bits.stride(0)
+    st = AttnStrides(_strides4(q), _strides4(k), _strides4(v), _strides4(out))
+    rc = _lib.dit_attn_fwd_masked_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(st), B, Nq, Nkv, H,
+                                          D, kvl, mask_bits.data_ptr(), sb, mask_bits.stride(1), rows, sc,
+                                          out.data_ptr(), DIT_F32 if out.dtype == torch.float32 else DIT_BF16,
+                                          lse.data_ptr(), _stream_ptr(stream))
+    _check(rc, "dit_attn_fwd_masked_noalloc")
     return out, lse
 
 

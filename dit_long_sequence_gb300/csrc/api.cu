@@ -20,6 +20,13 @@ namespace dit {
 // Device status word: [0] code, [1] block, [2] warp role, [3] wait site.
 __device__ unsigned int g_status_word[4];
 
+// Occupancy scratch of dit_attn_fwd_masked_noalloc: one per device, for
+// callers that cannot provide a workspace.  65,536 words cover every
+// configuration measured here (LTX-2 576 words, Wan 11,248, the 147,456-token
+// ring workload 20,736).
+constexpr int64_t kNoAllocOccWords = 65536;
+static __device__ __align__(256) uint32_t g_noalloc_occ[kNoAllocOccWords];
+
 namespace {
 
 constexpr unsigned long long kWatchdogNs = 2000000000ull;  // 2 s per bounded wait
@@ -46,6 +53,7 @@ EncodeTiledFn encode_fn() {
 struct DeviceCache {
     std::atomic<unsigned int*> status{nullptr};
     std::atomic<int> sm_count{0};
+    std::atomic<uint32_t*> noalloc_occ{nullptr};
 };
 DeviceCache g_dev[kMaxDevices];
 
@@ -57,6 +65,19 @@ unsigned int* status_word(int dev) {
         if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return nullptr;
         p = static_cast<unsigned int*>(addr);
         g_dev[dev].status.store(p, std::memory_order_release);
+    }
+    return p;
+}
+
+// Device address of the no-alloc occupancy scratch, looked up once per device.
+uint32_t* noalloc_scratch(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    uint32_t* p = g_dev[dev].noalloc_occ.load(std::memory_order_acquire);
+    if (p == nullptr) {
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_noalloc_occ) != cudaSuccess) return nullptr;
+        p = static_cast<uint32_t*>(addr);
+        g_dev[dev].noalloc_occ.store(p, std::memory_order_release);
     }
     return p;
 }
@@ -276,6 +297,22 @@ dit_status_t dit_attn_fwd_masked(const void* q, const void* k, const void* v, co
     const MaskSpec spec{mask, mask_batch_stride, mask_row_stride, mask_rows, static_cast<uint32_t*>(workspace)};
     return attn_fwd_common(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, scale, out, out_dtype, lse, false,
                            stream, nullptr, &spec);
+}
+
+dit_status_t dit_attn_fwd_masked_noalloc(const void* q, const void* k, const void* v,
+                                         const dit_attn_strides_t* strides, int B, int Nq, int Nkv, int H, int D,
+                                         int key_valid_len, const uint32_t* mask, int64_t mask_batch_stride,
+                                         int64_t mask_row_stride, int mask_rows, float scale, void* out,
+                                         dit_dtype_t out_dtype, float* lse, dit_stream_t stream) {
+    const int64_t need = (B > 0 && Nq > 0 && key_valid_len > 0) ? occ_bytes_of(B, Nq, key_valid_len) : 0;
+    if (need > kNoAllocOccWords * 4) return DIT_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DIT_ERR_CUDA;
+    uint32_t* scratch = noalloc_scratch(dev);
+    if (scratch == nullptr) return DIT_ERR_CUDA;
+    return dit_attn_fwd_masked(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, mask, mask_batch_stride,
+                               mask_row_stride, mask_rows, scale, out, out_dtype, lse, scratch,
+                               static_cast<size_t>(kNoAllocOccWords * 4), stream);
 }
 
 dit_status_t dit_attn_fwd_fp8(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides,

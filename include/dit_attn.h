@@ -147,6 +147,31 @@ dit_status_t dit_attn_fwd_masked(const void *q, const void *k, const void *v,
                                  dit_stream_t stream);
 
 /*
+ * dit_attn_fwd_masked_noalloc -- dit_attn_fwd_masked with its tile-occupancy
+ * scratch taken from a fixed array inside the library instead of a
+ * caller-provided workspace.  The pages have no counterpart: it serves callers
+ * that cannot allocate device memory at call time, e.g. an engine that hands
+ * all free device memory to its own pool at start-up, or a plain C host
+ * program with no device allocator of its own.
+ *
+ * Same arguments and results as dit_attn_fwd_masked without the workspace.
+ * Limits: one scratch array (65,536 words) per device and process, so
+ *   - DIT_ERR_UNSUPPORTED when dit_attn_masked_workspace_bytes(B, Nq,
+ *     key_valid_len) exceeds 262,144 bytes (checked before anything is enqueued);
+ *   - calls on one device must be ordered (the same stream, or streams joined
+ *     by events): two in flight at once would share the array.
+ * Allocates nothing; the array's address is looked up once per device.
+ */
+dit_status_t dit_attn_fwd_masked_noalloc(const void *q, const void *k, const void *v,
+                                         const dit_attn_strides_t *strides,
+                                         int B, int Nq, int Nkv, int H, int D,
+                                         int key_valid_len,
+                                         const uint32_t *mask, int64_t mask_batch_stride,
+                                         int64_t mask_row_stride, int mask_rows,
+                                         float scale, void *out, dit_dtype_t out_dtype, float *lse,
+                                         dit_stream_t stream);
+
+/*
  * dit_attn_masked_workspace_bytes -- bytes of `workspace` that let
  * dit_attn_fwd_masked skip key tiles the mask leaves empty: one bit per
  * (batch, 256-row query block, 128-key tile), written by a pre-pass on the
