@@ -155,3 +155,21 @@ def test_fp8_attention_sampled_rows_full_size(dl, name):
     Os, Ls = gather_rows(O, L, rows)
     vmax = _absmax(codes[:, :, 2]) * d
     compare_fp8(Os, Ls, Oref, Lref, vmax)
+
+
+@pytest.mark.parametrize("Nq,Nkv,kvl", [(300, 77, None), (513, 2048, 1999), (129, 129, 128)])
+def test_fp8_cross_attention_on_separate_tensors(dl, Nq, Nkv, kvl):
+    """Separate (non-stacked) E4M3 tensors, Nq != Nkv, padded row strides."""
+    B, H, D = 2, 2, 128
+    g = 60 + Nq
+    q8 = wl.randn_e4m3((B, Nq, H, D + 16), g, 64.0, DEV)[..., :D]
+    k8 = wl.randn_e4m3((B, Nkv, H, D), g + 1, 64.0, DEV)
+    v8 = wl.randn_e4m3((B, Nkv, H, D), g + 2, 64.0, DEV)
+    d = 1.0 / 64
+    O, L = dl.attn_fwd_fp8(q8, k8, v8, (d, d, d), key_valid_len=kvl)
+    torch.cuda.synchronize()
+    Oref, Lref = oracle.attn_fp8(host_u8(q8), host_u8(k8), host_u8(v8), scale=D ** -0.5, descale_q=d,
+                                 descale_k=d, descale_v=d, key_valid_len=kvl)
+    vmax = _absmax(host_u8(v8)) * d
+    compare_fp8(O.double().permute(0, 2, 1, 3).cpu().numpy(), L.double().cpu().numpy(),
+                Oref.transpose(0, 2, 1, 3), Lref, vmax)
