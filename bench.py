@@ -603,7 +603,7 @@ def main(argv=None):
     traffic = profiled_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": "attn_fwd_fp8_kernel<false>" if w.fp8 else "attn_fwd_kernel<128,false,false>",
+                "kernel": "attn_fwd_fp8_kernel<false>" if w.fp8 else "attn_fwd_kernel<128,false,false,false>",
                 "peak_kind": (f"{peak_kind} dense bf16 burst x 2 (nominal fp8/bf16 ratio)" if w.fp8
                               else f"{peak_kind} dense bf16 burst"),
                 "flops_per_launch": per_launch_flops, "ms_per_launch": attn_ms}
