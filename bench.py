@@ -31,6 +31,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -87,7 +88,7 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.t0 = self.t1 = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"dit_bench_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
