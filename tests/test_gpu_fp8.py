@@ -173,3 +173,38 @@ def test_fp8_cross_attention_on_separate_tensors(dl, Nq, Nkv, kvl):
     vmax = _absmax(host_u8(v8)) * d
     compare_fp8(O.double().permute(0, 2, 1, 3).cpu().numpy(), L.double().cpu().numpy(),
                 Oref.transpose(0, 2, 1, 3), Lref, vmax)
+
+
+def test_fp8_attention_sinks_and_long_tails(dl):
+    """Rows whose scores have four dominant keys (attention sinks) over thousands
+    of small ones: each sink sits ~13 units above a typical key in log2 terms, so
+    the sinks hold most of each row's mass (~70%) and the tail, at P ~2^-6 of the
+    row max, the rest -- which E4M3 must carry within the derived tolerance (the
+    mass split is asserted from the oracle's decoded inputs)."""
+    B, N, H, D = 1, 4096, 2, 128
+    g = wl.generator(DEV, 77)
+    x = torch.randn((B, N, 3, H, D), device=DEV, generator=g)
+    direction = torch.randn((D,), device=DEV, generator=g)
+    direction = direction / direction.norm()
+    x[:, :, 0] += 4.0 * direction                     # every query leans towards `direction`
+    x[:, :, 1, :, :] -= (x[:, :, 1] @ direction)[..., None] * direction   # keys orthogonal to it ...
+    x[:, 100:104, 1] += 24.0 * direction              # ... except four sinks
+    buf = x.to(torch.bfloat16)
+    scales = tuple(448.0 / float(buf[:, :, t].abs().max()) for t in range(3))
+    desc = tuple(1.0 / sc for sc in scales)
+    qkv8 = dl.qkv_cast_fp8(buf, scales)
+    O, L = dl.attn_fwd_fp8(*dl.split_stacked_fp8(qkv8), desc)
+    torch.cuda.synchronize()
+    codes = oracle.qkv_cast_fp8(_bits(buf), scales)
+    Oref, Lref = oracle.attn_fp8(codes[:, :, 0], codes[:, :, 1], codes[:, :, 2], scale=D ** -0.5,
+                                 descale_q=desc[0], descale_k=desc[1], descale_v=desc[2])
+    # the mass split this case is about: sinks hold most, the tail a large share
+    qd = oracle.e4m3_decode(codes[0, :64, 0, 0]) * desc[0]
+    kd = oracle.e4m3_decode(codes[0, :, 1, 0]) * desc[1]
+    sc = (qd @ kd.T) * D ** -0.5
+    w = np.exp(sc - sc.max(axis=1, keepdims=True))
+    sink_share = w[:, 100:104].sum(1) / w.sum(1)
+    assert 0.3 < np.median(sink_share) < 0.97, np.median(sink_share)
+    vmax = _absmax(codes[:, :, 2]) * desc[2]
+    compare_fp8(O.double().permute(0, 2, 1, 3).cpu().numpy(), L.double().cpu().numpy(), Oref.transpose(0, 2, 1, 3),
+                Lref, vmax)
