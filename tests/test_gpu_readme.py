@@ -1,0 +1,23 @@
+"""The Python example in README.md runs as written (every entry point it shows
+returns without error and gives finite results where rows have keys)."""
+import os
+import re
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_readme_example_runs():
+    text = open(os.path.join(ROOT, "README.md"), encoding="utf-8").read()
+    blocks = re.findall(r"```python\n(.*?)```", text, flags=re.S)
+    assert blocks, "README has no python example"
+    scope = {}
+    exec(compile(blocks[0], "README.md", "exec"), scope)
+    torch.cuda.synchronize()
+    for name in ("out", "merged", "run_o", "qn", "out8", "out_m"):
+        assert torch.isfinite(scope[name].float()).all(), name
+    rc, info = scope["dl"].check_watchdog()
+    assert rc == 0, info
