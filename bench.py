@@ -7,7 +7,9 @@ A step is one pass of the hot path over one batch of synthetic input.  For the
 default workload (ltx2_padded: B=1, H=32, D=128, 24,200 valid tokens padded to
 24,576, key-only mask) the step is: split the fused [B, T, 3, H, D] QKV
 projection into head-major Q/K/V (dit_qkv_to_head_major), then attention with
-LSE over the head-major views (dit_attn_fwd).  Other workloads: cosmos3_nano
+LSE over the head-major views (dit_attn_fwd_ws: dit_attn_fwd with a workspace
+that splits the grid's last partial wave over key ranges, plus the small
+kernel that merges those pieces).  Other workloads: cosmos3_nano
 (attention straight on strided views of the fused buffer), wan22_a14b
 (separate Q/K/V), ring9 (9 key chunks, 9 attention calls + dit_attn_lse_merge).
 
@@ -215,8 +217,16 @@ class Step:
             self.l_parts = torch.empty((n, B, H, N), dtype=torch.float32, device=dev)
         self.out = torch.empty((B, N, H, D), dtype=torch.float32, device=dev)
         self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        self.launches_per_step = {"layout+attn": 2, "attn": 1, "chunked+merge": w.kv_chunks + 1,
-                                  "cast+attn_fp8": 2}[self.mode]
+        # bf16 attention calls get the tail-split workspace (none when the plan has no split)
+        self.ws = None
+        if not w.fp8:
+            kvl_call = w.N // w.kv_chunks if self.mode == "chunked+merge" else w.kv_len
+            nb = dl.attn_fwd_workspace_bytes(B, N, H, D, kvl_call)
+            self.ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
+        # attention kernel (+ the split items' piece launch and the tail merge)
+        per_attn = 3 if self.ws is not None else 1
+        self.launches_per_step = {"layout+attn": 1 + per_attn, "attn": per_attn,
+                                  "chunked+merge": w.kv_chunks * per_attn + 1, "cast+attn_fp8": 2}[self.mode]
         self.attn_events = []
 
     def qkv_of(self, inputs):
@@ -260,12 +270,13 @@ class Step:
             n = w.kv_chunks
             cl = w.N // n
             for c in range(n):
-                dl.attn_fwd(q, k[:, c * cl:(c + 1) * cl], v[:, c * cl:(c + 1) * cl],
-                            out=self.o_parts[c], lse=self.l_parts[c], stream=stream)
+                dl.attn_fwd_ws(q, k[:, c * cl:(c + 1) * cl], v[:, c * cl:(c + 1) * cl],
+                               out=self.o_parts[c], lse=self.l_parts[c], workspace=self.ws, stream=stream)
         elif self.mode == "cast+attn_fp8":
             dl.attn_fwd_fp8(q, k, v, self.descales, key_valid_len=w.key_valid_len, out=out, lse=lse, stream=stream)
         else:
-            dl.attn_fwd(q, k, v, key_valid_len=w.key_valid_len, out=out, lse=lse, stream=stream)
+            dl.attn_fwd_ws(q, k, v, key_valid_len=w.key_valid_len, out=out, lse=lse, workspace=self.ws,
+                           stream=stream)
         if record:
             ev[1].record(stream)
             self.attn_events.append(ev)
@@ -608,6 +619,12 @@ def main(argv=None):
                 "peak_kind": (f"{peak_kind} dense bf16 burst x 2 (nominal fp8/bf16 ratio)" if w.fp8
                               else f"{peak_kind} dense bf16 burst"),
                 "flops_per_launch": per_launch_flops, "ms_per_launch": attn_ms}
+    if not w.fp8:
+        ws_bytes = 0 if step.ws is None else step.ws.numel()
+        roofline["timed"] = ("the dit_attn_fwd_ws call: attn_fwd_kernel" +
+                             (" (whole items and the split items' pieces) and attn_tail_merge_kernel" if ws_bytes
+                              else " (no tail split for this shape)"))
+        roofline["tail_split_workspace_bytes"] = ws_bytes
 
     # ---------------- secondary HBM-bound kernels
     extra = {}

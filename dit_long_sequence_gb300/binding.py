@@ -41,6 +41,11 @@ _vp, _i, _i64, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_floa
 _lib.dit_attn_fwd.restype = _i
 _lib.dit_attn_fwd.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
                               _vp, _i, _vp, _vp]
+_lib.dit_attn_fwd_ws.restype = _i
+_lib.dit_attn_fwd_ws.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
+                                 _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]
+_lib.dit_attn_fwd_workspace_bytes.restype = ctypes.c_size_t
+_lib.dit_attn_fwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
 _lib.dit_attn_fwd_accumulate.restype = _i
 _lib.dit_attn_fwd_accumulate.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
                                          _vp, _vp, _vp]
@@ -72,7 +77,7 @@ _lib.dit_check_watchdog.restype = _i
 _lib.dit_check_watchdog.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
 _lib.dit_version.restype = ctypes.c_uint32
 
-EXPORTS = ("dit_attn_fwd", "dit_attn_fwd_masked", "dit_attn_fwd_masked_noalloc", "dit_attn_masked_workspace_bytes",
+EXPORTS = ("dit_attn_fwd", "dit_attn_fwd_ws", "dit_attn_fwd_workspace_bytes", "dit_attn_fwd_masked", "dit_attn_fwd_masked_noalloc", "dit_attn_masked_workspace_bytes",
            "dit_attn_fwd_accumulate", "dit_attn_lse_merge", "dit_qkv_to_head_major",
            "dit_qkv_norm_rope_to_head_major", "dit_qkv_cast_fp8", "dit_attn_fwd_fp8", "dit_status_string",
            "dit_check_watchdog",
@@ -104,15 +109,7 @@ def _strides4(t: torch.Tensor) -> Strides4:
     return Strides4(*t.stride())
 
 
-def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, key_valid_len: int | None = None,
-             scale: float | None = None, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-             out_dtype: torch.dtype = torch.float32, stream=None):
-    """O = softmax(scale Q K^T) V and LSE, through `dit_attn_fwd`.
-
-    q [B, Nq, H, D], k/v [B, Nkv, H, D]: bf16 CUDA tensors with any strides whose
-    last dimension is contiguous (strided views of a fused QKV buffer work as is).
-    Returns (out [B, Nq, H, D] in out_dtype, lse [B, H, Nq] fp32).
-    """
+def _attn_args(q, k, v, key_valid_len, scale, out, lse, out_dtype):
     B, Nq, H, D = q.shape
     Nkv = k.shape[1]
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -131,10 +128,47 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, key_valid_len
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
     st = AttnStrides(_strides4(q), _strides4(k), _strides4(v), _strides4(out))
+    return B, Nq, Nkv, H, D, kvl, sc, out, lse, st
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, key_valid_len: int | None = None,
+             scale: float | None = None, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+             out_dtype: torch.dtype = torch.float32, stream=None):
+    """O = softmax(scale Q K^T) V and LSE, through `dit_attn_fwd`.
+
+    q [B, Nq, H, D], k/v [B, Nkv, H, D]: bf16 CUDA tensors with any strides whose
+    last dimension is contiguous (strided views of a fused QKV buffer work as is).
+    Returns (out [B, Nq, H, D] in out_dtype, lse [B, H, Nq] fp32).
+    """
+    B, Nq, Nkv, H, D, kvl, sc, out, lse, st = _attn_args(q, k, v, key_valid_len, scale, out, lse, out_dtype)
     rc = _lib.dit_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(st), B, Nq, Nkv, H, D, kvl,
                            sc, out.data_ptr(), DIT_F32 if out.dtype == torch.float32 else DIT_BF16,
                            lse.data_ptr(), _stream_ptr(stream))
     _check(rc, "dit_attn_fwd")
+    return out, lse
+
+
+def attn_fwd_workspace_bytes(B: int, Nq: int, H: int, D: int, key_valid_len: int) -> int:
+    """Workspace that lets attn_fwd_ws balance the grid's last wave (current device; 0: no split)."""
+    return int(_lib.dit_attn_fwd_workspace_bytes(int(B), int(Nq), int(H), int(D), int(key_valid_len)))
+
+
+def attn_fwd_ws(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, key_valid_len: int | None = None,
+                scale: float | None = None, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                out_dtype: torch.dtype = torch.float32, workspace: torch.Tensor | None = None, stream=None):
+    """attn_fwd through `dit_attn_fwd_ws`: the items of the grid's last partial
+    wave are split over key ranges and merged.  The workspace (a uint8 CUDA
+    tensor of attn_fwd_workspace_bytes) is allocated here unless given."""
+    B, Nq, Nkv, H, D, kvl, sc, out, lse, st = _attn_args(q, k, v, key_valid_len, scale, out, lse, out_dtype)
+    if workspace is None:
+        nbytes = attn_fwd_workspace_bytes(B, Nq, H, D, kvl)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device) if nbytes else None
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = _lib.dit_attn_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(st), B, Nq, Nkv, H, D, kvl,
+                              sc, out.data_ptr(), DIT_F32 if out.dtype == torch.float32 else DIT_BF16,
+                              lse.data_ptr(), ws_ptr, ws_bytes, _stream_ptr(stream))
+    _check(rc, "dit_attn_fwd_ws")
     return out, lse
 
 

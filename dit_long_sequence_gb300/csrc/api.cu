@@ -155,7 +155,8 @@ int64_t occ_bytes_of(int B, int Nq, int key_valid_len) {
 dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides, int B,
                              int Nq, int Nkv, int H, int D, int key_valid_len, float scale, void* out,
                              dit_dtype_t out_dtype, float* lse, bool accumulate, dit_stream_t stream,
-                             const float* descales = nullptr, const MaskSpec* mask = nullptr) {
+                             const float* descales = nullptr, const MaskSpec* mask = nullptr,
+                             void* workspace = nullptr, size_t workspace_bytes = 0) {
     const bool fp8 = descales != nullptr;
     if (strides == nullptr) return DIT_ERR_INVALID_ARG;
     if (B < 0 || Nq < 0 || Nkv < 0 || H < 0) return DIT_ERR_INVALID_ARG;
@@ -202,6 +203,15 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DIT_ERR_CUDA;
+    // Work items (b, h, 256-row block) of the 1-D bf16 grid, and the tail split
+    // when the caller gave a workspace for it (plain, unmasked, overwrite only).
+    const int64_t items = static_cast<int64_t>(B) * H * ((static_cast<int64_t>(Nq) + 255) / 256);
+    SplitPlan split{items, 1, 0};
+    if (workspace != nullptr && !fp8 && !accumulate && mask == nullptr && any_keys) {
+        split = plan_tail_split(items, (key_valid_len + 127) / 128, device_sm_count(dev));
+        if (workspace_bytes < static_cast<size_t>(split_workspace_bytes(split, D))) return DIT_ERR_INVALID_ARG;
+        if (!aligned16(workspace)) return DIT_ERR_ALIGNMENT;
+    }
     AttnArgs a;
     a.status = status_word(dev);
     a.timeout_ns = kWatchdogNs;
@@ -246,10 +256,18 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
     a.o_sn = so.n;
     a.o_sh = so.h;
     a.lse = lse;
-    cudaError_t e = fp8 ? launch_attn_fwd_fp8(tq, tk, tv, a, B, out_dtype == DIT_BF16,
-                                              reinterpret_cast<cudaStream_t>(stream))
-                        : launch_attn_fwd(tq, tk, tv, a, B, D, out_dtype == DIT_BF16, accumulate,
-                                          reinterpret_cast<cudaStream_t>(stream));
+    a.n_qblk = static_cast<int>((static_cast<int64_t>(Nq) + 255) / 256);
+    a.split_first = static_cast<int>(split.first);
+    a.split_f = split.f;
+    a.n_split_ctas = static_cast<int>(split.n_ctas);
+    a.ws_o = split.n_ctas > 0 ? static_cast<float*>(workspace) : nullptr;
+    a.ws_lse = split.n_ctas > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                          split.n_ctas * 256 * D * 4)
+                                : nullptr;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = fp8 ? launch_attn_fwd_fp8(tq, tk, tv, a, B, out_dtype == DIT_BF16, cs)
+                        : launch_attn_fwd(tq, tk, tv, a, B, D, out_dtype == DIT_BF16, accumulate, cs);
+    if (e == cudaSuccess && !fp8) e = launch_attn_tail_merge(a, D, out_dtype == DIT_BF16, cs);
     return e == cudaSuccess ? DIT_OK : DIT_ERR_CUDA;
 }
 
@@ -262,6 +280,23 @@ dit_status_t dit_attn_fwd(const void* q, const void* k, const void* v, const dit
                           dit_dtype_t out_dtype, float* lse, dit_stream_t stream) {
     return attn_fwd_common(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, scale, out, out_dtype, lse, false,
                            stream);
+}
+
+size_t dit_attn_fwd_workspace_bytes(int B, int Nq, int H, int D, int key_valid_len) {
+    if (B <= 0 || Nq <= 0 || H <= 0 || key_valid_len <= 0 || (D != 64 && D != 128)) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const int64_t items = static_cast<int64_t>(B) * H * ((static_cast<int64_t>(Nq) + 255) / 256);
+    const SplitPlan p = plan_tail_split(items, (key_valid_len + 127) / 128, device_sm_count(dev));
+    return static_cast<size_t>(split_workspace_bytes(p, D));
+}
+
+dit_status_t dit_attn_fwd_ws(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides, int B,
+                             int Nq, int Nkv, int H, int D, int key_valid_len, float scale, void* out,
+                             dit_dtype_t out_dtype, float* lse, void* workspace, size_t workspace_bytes,
+                             dit_stream_t stream) {
+    return attn_fwd_common(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, scale, out, out_dtype, lse, false,
+                           stream, nullptr, nullptr, workspace, workspace_bytes);
 }
 
 dit_status_t dit_attn_fwd_accumulate(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides,

@@ -11,7 +11,8 @@
 // The key-only tail mask follows "8 卡怎么分 token：LTX-2 序列并行的 all2all
 // 到底搬了什么" ("构造 padding mask").
 //
-// CTA = 256 query rows of one (b, h) as two 128-row tiles, 12 warps:
+// CTA = 256 query rows of one (b, h) -- a work item -- as two 128-row tiles,
+// 12 warps:
 //   warps 0-3  softmax for query tile 0 (one TMEM lane = one row per thread)
 //   warps 4-7  softmax for query tile 1
 //   warp  8    tcgen05.mma issuer (one thread); owns the TMEM allocation
@@ -43,6 +44,21 @@
 // Keys j >= kv_len are outside the K/V tensor maps (zero fill) and masked to
 // -inf in the last tile, so pad rows are never read.
 //
+// Grid: (256-row blocks, H, B), one CTA per work item.  With a workspace the
+// items of the last partial wave (items mod SMs of them, the last in grid
+// order) are left by this grid to a second launch of the same kernel body
+// (PIECE) that runs each of them as f key-range pieces.  That launch is a
+// programmatic dependent launch: every CTA here signals at its start, so the
+// pieces may be scheduled once the last whole item has begun, and they take
+// SMs as the last whole items drain -- the end of the work is balanced at
+// 1/f of an item's time instead of a whole item (SMs also differ in speed by
+// ~1-2%, which a fine-grained end absorbs too).  Each piece writes its
+// normalised partial O and LSE to the workspace, and attn_tail_merge_kernel
+// combines each item's f partials exactly as the (O, LSE) merge does.  The
+// whole-item kernel is compiled without any of the piece logic: its softmax
+// loop sits at the edge of its register budget, where one more value held
+// across the loop costs ~2% of the loop's time.
+//
 // MASK variant: a general (B, T, T) mask -- one bit per (query, key), shared by
 // the heads -- also sets masked scores to -inf; rows i >= mask_rows attend every
 // valid key (the pad-row rule of "8 卡怎么分 token", "构造 padding mask").  Each
@@ -71,8 +87,8 @@ struct TileCursor {
     int n_words, n, w;
     uint32_t bits;
     int next_all;
-    __device__ TileCursor(const uint32_t* occ, int n_tiles)
-        : words(occ), n_words((n_tiles + 31) / 32), n(n_tiles), w(0), bits(occ ? occ[0] : 0u), next_all(0) {}
+    __device__ TileCursor(const uint32_t* occ, int begin, int end)
+        : words(occ), n_words((end + 31) / 32), n(end), w(0), bits(occ ? occ[0] : 0u), next_all(begin) {}
     // The next key tile to process, or -1.
     __device__ int next() {
         if (words == nullptr) return next_all < n ? next_all++ : -1;
@@ -124,7 +140,9 @@ struct Cfg {
 
 // ACCUM: fold this pass into an existing fp32 (O, LSE) pair instead of
 // overwriting it (streaming merge over key chunks).  MASK: apply the bit mask.
-template <int D, bool OUT_BF16, bool ACCUM, bool MASK>
+// PIECE: the kernel of the split items' key-range pieces (1-D grid, partials
+// to the workspace); the whole-item kernel is compiled without any of it.
+template <int D, bool OUT_BF16, bool ACCUM, bool MASK, bool PIECE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
@@ -145,14 +163,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int h = blockIdx.y;
-    const int b = blockIdx.z;
-    const int q_row0 = blockIdx.x * (2 * kBM);
+    // Work item of this CTA: (256-row block, head, batch) = (x, y, z) for a
+    // whole item; a piece decodes its item and key range from its 1-D index
+    // (items counted block fastest, then head, then batch).
+    static_assert(!PIECE || (!ACCUM && !MASK), "only plain overwriting passes are split");
+    struct W { int h, b, q_row0, qblk; };
+    int k_begin = 0, k_end = a.n_kv_tiles;   // key tiles [k_begin, k_end) of this CTA
+    auto item_w = [&]() {
+        W w;
+        if constexpr (PIECE) {
+            const int slot = static_cast<int>(blockIdx.x);
+            const int piece = slot % a.split_f;
+            const int item = a.split_first + slot / a.split_f;
+            k_begin = static_cast<int>(static_cast<int64_t>(piece) * a.n_kv_tiles / a.split_f);
+            k_end = static_cast<int>(static_cast<int64_t>(piece + 1) * a.n_kv_tiles / a.split_f);
+            w.qblk = item % a.n_qblk;
+            w.h = (item / a.n_qblk) % a.H;
+            w.b = item / a.n_qblk / a.H;
+        } else {
+            w.qblk = blockIdx.x;
+            w.h = blockIdx.y;
+            w.b = blockIdx.z;
+        }
+        w.q_row0 = w.qblk * (2 * kBM);
+        return w;
+    };
+    const W wk = item_w();
+    const int h = wk.h;
+    const int b = wk.b;
+    const int q_row0 = wk.q_row0;
+    if constexpr (!PIECE && !ACCUM && !MASK) {
+        // The piece kernel (if any) may start once every CTA here has begun;
+        // the items it covers are the last in grid order and left to it.
+        if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        if (static_cast<int>(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)) >= a.split_first) return;
+    }
     // MASK with an occupancy map: this CTA's row of tile bits
     const uint32_t* occ = (MASK && a.occ != nullptr)
                               ? a.occ + (static_cast<int64_t>(b) * gridDim.x + blockIdx.x) * a.occ_words
                               : nullptr;
-    const int n_tiles = count_tiles(occ, a.n_kv_tiles);   // key tiles this CTA processes
+    const int n_tiles = PIECE ? k_end - k_begin : count_tiles(occ, a.n_kv_tiles);   // key tiles this CTA processes
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::kQFull + 0), 1);
@@ -202,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int total = 2 * n_tiles;
             int issued = 0;
-            TileCursor cur(occ, a.n_kv_tiles);
+            TileCursor cur(occ, k_begin, k_end);
             int key0 = 0;
             for (int i = 0; i < total; ++i) {
                 if ((i & 1) == 0) key0 = cur.next() * kBN;
@@ -320,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_masked = MASK && row < a.mask_rows;
         const uint32_t* mrow = MASK ? a.mask + static_cast<int64_t>(b) * a.mask_sb + static_cast<int64_t>(row_masked ? row : 0) * a.mask_si
                                     : nullptr;
-        TileCursor cur(occ, a.n_kv_tiles);
+        TileCursor cur(occ, k_begin, k_end);
         int tile_next = n_tiles > 0 ? cur.next() : -1;   // key tile of the next iteration
         uint4 mw = make_uint4(~0u, ~0u, ~0u, ~0u);
         if (MASK && row_masked && n_tiles > 0) mw = __ldg(reinterpret_cast<const uint4*>(mrow) + tile_next);
@@ -474,8 +524,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
             static_assert(!(ACCUM && OUT_BF16), "accumulation keeps O in fp32");
             const bool in_range = row < a.Nq;
-            const int64_t o_off = static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(row) * a.o_sn +
-                                  static_cast<int64_t>(h) * a.o_sh;
             const int64_t lse_idx = (static_cast<int64_t>(b) * a.H + h) * a.Nq + row;
             const bool any_key = n_tiles > 0 && (!MASK || l > 0.f);
             const float lse_new = any_key ? (m + log2f(l)) * kLn2 : -INFINITY;
@@ -500,7 +548,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     lse_out = mx + logf(wp + wn);
                 }
             }
-#pragma unroll
+            // Each 32-column chunk goes through this warp's 4 KB of the Q_t buffer
+            // (idle since QK_t(last) completed, which S_t(last) signalled): a
+            // thread writes its row, then the warp stores four rows per
+            // instruction as whole 128-byte lines instead of 32 scattered pieces.
+            // Rows sit 128 bytes apart with the 16-byte groups XOR-swizzled by
+            // the row, so both phases are free of bank conflicts.
+            float4* stg = reinterpret_cast<float4*>(smem + t * TILE + wq * 4096);
+            const int k4 = lane & 7;        // 16-byte group this lane moves in the store phase
+            const int r_sub = lane >> 3;    // row within each group of four
+            float* const out_f = static_cast<float*>(a.out);
+            uint16_t* const out_h = static_cast<uint16_t*>(a.out);
+#pragma unroll 1
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
                 if (n_tiles > 0) {
@@ -510,37 +569,49 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = 0u;
                 }
-                if (in_range) {
-                    if constexpr (OUT_BF16) {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + o_off + cc * 32);
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * c_new, __uint_as_float(o[8 * v4 + 1]) * c_new);
-                            w.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * c_new, __uint_as_float(o[8 * v4 + 3]) * c_new);
-                            w.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * c_new, __uint_as_float(o[8 * v4 + 5]) * c_new);
-                            w.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * c_new, __uint_as_float(o[8 * v4 + 7]) * c_new);
-                            dst[v4] = w;
-                        }
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + o_off + cc * 32);
+                for (int v4 = 0; v4 < 8; ++v4)
+                    stg[lane * 8 + (v4 ^ (lane & 7))] =
+                        make_float4(__uint_as_float(o[4 * v4 + 0]) * c_new, __uint_as_float(o[4 * v4 + 1]) * c_new,
+                                    __uint_as_float(o[4 * v4 + 2]) * c_new, __uint_as_float(o[4 * v4 + 3]) * c_new);
+                __syncwarp();
 #pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4) {
-                            float4 r = make_float4(__uint_as_float(o[4 * v4 + 0]) * c_new, __uint_as_float(o[4 * v4 + 1]) * c_new,
-                                                   __uint_as_float(o[4 * v4 + 2]) * c_new, __uint_as_float(o[4 * v4 + 3]) * c_new);
-                            if (ACCUM && c_prev > 0.f) {
-                                const float4 pv = dst[v4];
-                                r.x = fmaf(c_prev, pv.x, r.x);
-                                r.y = fmaf(c_prev, pv.y, r.y);
-                                r.z = fmaf(c_prev, pv.z, r.z);
-                                r.w = fmaf(c_prev, pv.w, r.w);
+                for (int it = 0; it < 8; ++it) {
+                    const int r = it * 4 + r_sub;                   // row within the warp's 32
+                    float4 val = stg[r * 8 + (k4 ^ (r & 7))];
+                    const float cp = ACCUM ? __shfl_sync(0xffffffffu, c_prev, r) : 0.f;
+                    const int grow = q_row0 + t * kBM + wq * 32 + r;
+                    if (PIECE && grow < a.Nq) {
+                        // a piece's fp32 partial, row-major [256][D] in its workspace slot
+                        *reinterpret_cast<float4*>(a.ws_o + (static_cast<int64_t>(blockIdx.x) * (2 * kBM) + (grow - q_row0)) * D +
+                                                   cc * 32 + 4 * k4) = val;
+                    } else if (grow < a.Nq) {
+                        const int64_t off = static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(grow) * a.o_sn +
+                                            static_cast<int64_t>(h) * a.o_sh + cc * 32 + 4 * k4;
+                        if constexpr (OUT_BF16) {
+                            *reinterpret_cast<uint2*>(out_h + off) =
+                                make_uint2(pack_bf16x2(val.x, val.y), pack_bf16x2(val.z, val.w));
+                        } else {
+                            float4* dst = reinterpret_cast<float4*>(out_f + off);
+                            if (ACCUM && cp > 0.f) {
+                                const float4 pv = *dst;
+                                val.x = fmaf(cp, pv.x, val.x);
+                                val.y = fmaf(cp, pv.y, val.y);
+                                val.z = fmaf(cp, pv.z, val.z);
+                                val.w = fmaf(cp, pv.w, val.w);
                             }
-                            dst[v4] = r;
+                            *dst = val;
                         }
                     }
                 }
+                __syncwarp();
             }
-            if (in_range) a.lse[lse_idx] = lse_out;
+            if (in_range) {
+                if (PIECE)
+                    a.ws_lse[static_cast<int64_t>(blockIdx.x) * (2 * kBM) + (row - q_row0)] = lse_out;
+                else
+                    a.lse[lse_idx] = lse_out;
+            }
         }
     }
 
@@ -550,6 +621,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    // A piece completes only after the whole-item grid it was launched beside
+    // (whose outputs are the stream's too); by then that grid has no CTA left
+    // to schedule, so the wait holds nothing back.
+    if constexpr (PIECE) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int D, bool BF16, bool ACCUM, bool MASK = false>
@@ -559,12 +634,100 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     const int smem = Cfg<D>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((args.Nq + 2 * kBM - 1) / (2 * kBM), args.H, B);
+    const dim3 grid(args.n_qblk, args.H, B);
     kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, args);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess || ACCUM || MASK || args.n_split_ctas == 0) return e;
+    // The split items' pieces: a programmatic dependent launch, so that its
+    // CTAs take SMs as the last whole items drain instead of after the grid.
+    auto piece = attn_fwd_kernel<D, BF16, false, false, true>;
+    e = cudaFuncSetAttribute(piece, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(args.n_split_ctas));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, piece, tq, tk, tv, args);
+}
+
+// Combine the split pieces: per (split item, row) the f normalised partials
+// (O_p, LSE_p) give O = sum_p w_p O_p, LSE = M + ln sum_p e^(LSE_p - M), with
+// w_p = e^(LSE_p - M) / sum_q e^(LSE_q - M) and M = max_p LSE_p.  Every piece
+// covers at least one valid key, so each LSE_p is finite.  D/4 lanes per row,
+// one float4 of O each: coalesced reads of the row-major partials and of the
+// output row.
+template <int D, bool OUT_BF16>
+__global__ void __launch_bounds__(256) attn_tail_merge_kernel(const AttnArgs a) {
+    constexpr int LPR = D / 4;
+    const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t unit = g / LPR;                     // (split item, row)
+    const int c4 = static_cast<int>(g % LPR);
+    const int f = a.split_f;
+    if (unit >= static_cast<int64_t>(a.n_split_ctas / f) * (2 * kBM)) return;
+    const int it = static_cast<int>(unit / (2 * kBM));
+    const int r = static_cast<int>(unit % (2 * kBM));
+    const int item = a.split_first + it;
+    const int qblk = item % a.n_qblk;
+    const int h = (item / a.n_qblk) % a.H;
+    const int b = item / a.n_qblk / a.H;
+    const int grow = qblk * (2 * kBM) + r;
+    if (grow >= a.Nq) return;
+    const int64_t piece0 = static_cast<int64_t>(it) * f;
+    float lp[kMaxSplit];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int p = 0; p < kMaxSplit; ++p) {
+        lp[p] = p < f ? a.ws_lse[(piece0 + p) * (2 * kBM) + r] : -INFINITY;
+        mx = fmaxf(mx, lp[p]);
+    }
+    float wsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int p = 0; p < kMaxSplit; ++p) {
+        if (p < f) {
+            const float w = expf(lp[p] - mx);
+            wsum += w;
+            const float4 o = __ldcs(reinterpret_cast<const float4*>(a.ws_o + ((piece0 + p) * (2 * kBM) + r) * D) + c4);
+            acc.x = fmaf(w, o.x, acc.x);
+            acc.y = fmaf(w, o.y, acc.y);
+            acc.z = fmaf(w, o.z, acc.z);
+            acc.w = fmaf(w, o.w, acc.w);
+        }
+    }
+    const float inv = 1.f / wsum;
+    const int64_t off = static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(grow) * a.o_sn +
+                        static_cast<int64_t>(h) * a.o_sh + 4 * c4;
+    if constexpr (OUT_BF16) {
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + off) =
+            make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + off) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+    if (c4 == 0) a.lse[(static_cast<int64_t>(b) * a.H + h) * a.Nq + grow] = mx + logf(wsum);
 }
 
 }  // namespace
+
+cudaError_t launch_attn_tail_merge(const AttnArgs& args, int D, bool out_bf16, cudaStream_t stream) {
+    if (args.n_split_ctas == 0) return cudaSuccess;
+    const int64_t threads = static_cast<int64_t>(args.n_split_ctas / args.split_f) * (2 * kBM) * (D / 4);
+    const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+    if (D == 128) {
+        if (out_bf16) attn_tail_merge_kernel<128, true><<<blocks, 256, 0, stream>>>(args);
+        else attn_tail_merge_kernel<128, false><<<blocks, 256, 0, stream>>>(args);
+    } else {
+        if (out_bf16) attn_tail_merge_kernel<64, true><<<blocks, 256, 0, stream>>>(args);
+        else attn_tail_merge_kernel<64, false><<<blocks, 256, 0, stream>>>(args);
+    }
+    return cudaGetLastError();
+}
 
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const AttnArgs& args, int B, int D, bool out_bf16, bool accumulate, cudaStream_t stream) {
@@ -587,3 +750,4 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
 }
 
 }  // namespace dit
+

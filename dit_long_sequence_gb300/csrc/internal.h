@@ -32,14 +32,69 @@ struct AttnArgs {
     int occ_words;
     unsigned int* status;      // device status word (4 x u32)
     unsigned long long timeout_ns;
+    // Work items are (b, h, 256-row block), counted block fastest, then head,
+    // then batch (the bf16 kernel's grid order).  Items >= split_first (the
+    // last partial wave) are each split into split_f key ranges run by a
+    // second, 1-D launch (piece slot = (item - split_first) * split_f + piece)
+    // that writes normalised partials (O, LSE) to ws_o [slot][256][D] and
+    // ws_lse [slot][256]; launch_attn_tail_merge combines them into out / lse.
+    // No split: split_first = items, split_f = 1, n_split_ctas = 0.  Unused by
+    // the FP8 kernel.
+    int n_qblk;                // ceil(Nq / 256)
+    int split_first;
+    int split_f;
+    int n_split_ctas;          // (items - split_first) * split_f
+    float* ws_o;
+    float* ws_lse;
 };
 
-// Attention forward.  grid = (ceil(Nq/256), H, B), 384 threads.  accumulate:
-// merge into the fp32 (out, lse) already there instead of overwriting them.
+// Tail split of the bf16 attention grid: the last partial wave's items
+// (tail = items % sms of them) are cut into f = sms / tail key ranges (one
+// wave of pieces when the grid has no whole wave), at least 2 and at most
+// kMaxSplit, each range at least kMinSplitTiles key tiles; no split when even
+// 2 ranges would be shorter.
+struct SplitPlan {
+    int64_t first;   // items before the split ones
+    int f;           // pieces per split item (1 = no split)
+    int64_t n_ctas;  // pieces in total
+};
+constexpr int kMaxSplit = 8;
+constexpr int kMinSplitTiles = 16;
+inline SplitPlan plan_tail_split(int64_t items, int n_kv_tiles, int sms) {
+    SplitPlan p{items, 1, 0};
+    if (sms <= 0 || n_kv_tiles <= 0 || items <= 0) return p;
+    const int64_t tail = items % sms;
+    if (tail == 0) return p;
+    int64_t f = sms / tail;
+    if (f < 2) f = 2;
+    if (f > kMaxSplit) f = kMaxSplit;
+    if (f > n_kv_tiles / kMinSplitTiles) f = n_kv_tiles / kMinSplitTiles;
+    if (f < 2) return p;
+    p.first = items - tail;
+    p.f = static_cast<int>(f);
+    p.n_ctas = tail * f;
+    return p;
+}
+// Workspace bytes of a plan: partial O then partial LSE, 256-byte aligned parts.
+inline int64_t split_workspace_bytes(const SplitPlan& p, int D) {
+    if (p.n_ctas == 0) return 0;
+    const int64_t o_bytes = p.n_ctas * 256 * D * 4;
+    const int64_t l_bytes = (p.n_ctas * 256 * 4 + 255) / 256 * 256;
+    return o_bytes + l_bytes;
+}
+
+// Attention forward.  grid = (ceil(Nq/256), H, B), 384 threads, plus the
+// split items' pieces (n_split_ctas CTAs) as a programmatic dependent launch.
+// accumulate: merge into the fp32 (out, lse) already there instead of
+// overwriting them (no split).
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const AttnArgs& args, int B, int D, bool out_bf16, bool accumulate, cudaStream_t stream);
 
-// FP8 (E4M3) attention forward, D = 128.  Same grid and roles as the bf16
+// Combine of the split pieces' partials into out / lse (after launch_attn_fwd
+// on the same stream).  Nothing to do when args.n_split_ctas == 0.
+cudaError_t launch_attn_tail_merge(const AttnArgs& args, int D, bool out_bf16, cudaStream_t stream);
+
+// FP8 (E4M3) attention forward, D = 128.  Grid (ceil(Nq/256), H, B); the roles of the bf16
 // kernel; scale_log2 already includes the Q and K descales.
 cudaError_t launch_attn_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const AttnArgs& args, int B, bool out_bf16, cudaStream_t stream);

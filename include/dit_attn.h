@@ -7,6 +7,8 @@
  *   dit_attn_fwd           softmax(scale * Q K^T) V plus the per-row
  *                          log-sum-exp, Q/K/V read through arbitrary
  *                          (b, n, h) strides, key-only padding mask.
+ *   dit_attn_fwd_ws        the same with a workspace that balances the
+ *                          grid's last partial wave.
  *   dit_attn_fwd_masked    the same with a general (B, Nq, Nkv) bit mask.
  *   dit_attn_lse_merge     exact combine of (O, LSE) partials computed over
  *                          disjoint key chunks.
@@ -103,6 +105,48 @@ dit_status_t dit_attn_fwd(const void *q, const void *k, const void *v,
                           int key_valid_len, float scale,
                           void *out, dit_dtype_t out_dtype, float *lse,
                           dit_stream_t stream);
+
+/*
+ * dit_attn_fwd_ws -- dit_attn_fwd with a caller workspace that balances the
+ * last wave of the grid.
+ *
+ * The GPU runs one CTA per (b, h, 256-row query block) work item.  When the
+ * item count is not a multiple of the SM count, the last partial wave leaves
+ * most SMs idle for a whole item's time.  With a workspace, each item of that
+ * partial wave is split into f contiguous key ranges (f = SMs / leftover items
+ * clamped to [2, 8], at least 16 key tiles of 128 each), run by a second
+ * kernel launched as a programmatic dependent launch so that its CTAs fill the
+ * SMs as the last whole items drain, and their normalised partial (O, LSE)
+ * pairs are combined by a third kernel with the
+ * exact merge of "Scaling Video Generation Across NVL72 rack with
+ * TensorRT-LLM", "Ring Attention", paragraph "Online-softmax merge" (the pages
+ * have no counterpart for the scheduling itself; the combine is that merge).
+ * Results equal dit_attn_fwd's up to fp32 rounding of the merge.
+ *
+ * workspace  NULL (then exactly dit_attn_fwd), or device memory of at least
+ *        dit_attn_fwd_workspace_bytes(B, Nq, H, D, key_valid_len) bytes, 16-byte
+ *        aligned, owned by the caller and not used by anything else until the
+ *        stream has passed the call.  A smaller non-zero size is
+ *        DIT_ERR_INVALID_ARG.
+ * Other arguments and results as dit_attn_fwd.  Enqueues one kernel, or three
+ * when a split applies.
+ */
+dit_status_t dit_attn_fwd_ws(const void *q, const void *k, const void *v,
+                             const dit_attn_strides_t *strides,
+                             int B, int Nq, int Nkv, int H, int D,
+                             int key_valid_len, float scale,
+                             void *out, dit_dtype_t out_dtype, float *lse,
+                             void *workspace, size_t workspace_bytes,
+                             dit_stream_t stream);
+
+/*
+ * dit_attn_fwd_workspace_bytes -- workspace bytes dit_attn_fwd_ws uses for this
+ * shape on the CURRENT device (the plan depends on its SM count): the split
+ * pieces' fp32 partial O (256 x D per piece) and LSE (256 per piece).  0 when
+ * no split helps (the item count is a multiple of the SM count, the keys are
+ * too few, or there is nothing to compute); D outside {64, 128} gives 0.
+ */
+size_t dit_attn_fwd_workspace_bytes(int B, int Nq, int H, int D, int key_valid_len);
 
 /*
  * dit_attn_fwd_masked -- dit_attn_fwd with a general attention mask.

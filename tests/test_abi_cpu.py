@@ -214,3 +214,22 @@ def test_masked_argument_checks(lib):
     ws = lib.raw().dit_attn_masked_workspace_bytes
     assert ws(1, 24576, 24200) == 96 * 6 * 4                   # 96 row blocks x 190 tiles -> 6 words
     assert ws(2, 256, 128) == 8 and ws(0, 10, 10) == 0 and ws(1, 10, 0) == 0
+
+
+def test_attn_fwd_ws_argument_checks(lib):
+    st = lib.AttnStrides(*(lib.Strides4(8 * 128 * 4, 4 * 128, 128, 1) for _ in range(4)))
+    f = lib.raw().dit_attn_fwd_ws
+
+    def call(D=128, kvl=8, scale=0.088, out=FAKE, B=1):
+        return f(FAKE, FAKE, FAKE, ctypes.byref(st), B, 8, 8, 4, D, kvl, scale, out, lib.DIT_F32, FAKE,
+                 FAKE, 1 << 20, None)
+    # the checks shared with dit_attn_fwd run first, whatever the workspace
+    assert call(D=96) == lib.DIT_ERR_UNSUPPORTED
+    assert call(kvl=9) == lib.DIT_ERR_INVALID_ARG
+    assert call(scale=0.0) == lib.DIT_ERR_INVALID_ARG
+    assert call(out=None) == lib.DIT_ERR_INVALID_ARG
+    assert call(out=FAKE + 4) == lib.DIT_ERR_ALIGNMENT
+    assert call(B=0) == lib.DIT_OK
+    wsb = lib.raw().dit_attn_fwd_workspace_bytes
+    assert wsb(1, 24576, 32, 96, 24200) == 0          # unsupported D
+    assert wsb(0, 24576, 32, 128, 24200) == 0 and wsb(1, 24576, 32, 128, 0) == 0

@@ -1,0 +1,200 @@
+"""GPU checks of dit_attn_fwd_ws: the work items of the grid's last partial
+wave split over key ranges, their partial (O, LSE) merged by a second kernel.
+
+- the plan (pieces per split item) follows its rule for this GPU's SM count;
+- shapes where every item is split (f = 2, 3, 8; ragged query blocks and key
+  tiles; D = 64 and 128; fp32 and bf16 output) match the fp64 oracle whole;
+- items that are not split are bit-identical to dit_attn_fwd; split ones
+  differ from it by the bf16 rounding of P (a piece rounds its probabilities
+  against its own running max, so they round differently: about
+  2^-8 * |v| / sqrt(keys) per element, a few 1e-4 at most at 8k keys; the
+  LSE only by fp32 rounding);
+- a NULL workspace is exactly dit_attn_fwd; a short one is refused before
+  anything is enqueued;
+- the LTX-2-shaped workload in the benchmark's configuration (32 items of
+  head 31 split 4 ways on a 152-SM GB300) matches the oracle on sampled rows
+  that include the split rows.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from dit_long_sequence_gb300 import workloads as wl
+import parity
+
+pytestmark = pytest.mark.gpu
+
+SPLIT_VS_SINGLE_O = 2e-3      # ~10x the largest difference seen at 8k keys
+SPLIT_VS_SINGLE_LSE = 5e-5
+
+
+def _dev():
+    return torch.device("cuda:0")
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _plan(B, Nq, H, kvl):
+    """Pieces per split item and the index of the first split item: the tail
+    of items mod SMs, cut into f = min(max(SMs // tail, 2), 8, key tiles // 16)
+    ranges when f >= 2."""
+    items = B * H * ((Nq + 255) // 256)
+    tiles = (kvl + 127) // 128
+    tail = items % _sms()
+    if tail == 0 or tiles == 0:
+        return 1, items
+    f = min(max(_sms() // tail, 2), 8, tiles // 16)
+    return (f, items - tail) if f >= 2 else (1, items)
+
+
+def _expected_bytes(B, Nq, H, D, kvl):
+    f, first = _plan(B, Nq, H, kvl)
+    items = B * H * ((Nq + 255) // 256)
+    pieces = (items - first) * f
+    if f == 1:
+        return 0
+    return pieces * 256 * D * 4 + (pieces * 256 * 4 + 255) // 256 * 256
+
+
+def _split_rows_mask(B, Nq, H, kvl):
+    """[B, H, Nq] bool: rows that belong to split items."""
+    f, first = _plan(B, Nq, H, kvl)
+    nqb = (Nq + 255) // 256
+    m = np.zeros((B, H, Nq), dtype=bool)
+    for item in range(first, B * H * nqb):
+        qb, h, b = item % nqb, (item // nqb) % H, item // nqb // H
+        m[b, h, qb * 256:min(Nq, qb * 256 + 256)] = True
+    return m
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 24576, 32, 128, 24200),    # LTX-2-shaped
+    (2, 44160, 16, 128, 44160),    # Cosmos-shaped
+    (2, 75600, 40, 128, 75600),    # Wan-shaped
+    (1, 60000, 40, 128, 300),      # 3 key tiles: too few to split
+    (1, 1024, 2, 64, 1024),        # tiny: too few key tiles
+    (1, 8192, 2, 128, 8000),
+    (1, 2048, 2, 128, 16384),
+    (1, 6400, 2, 128, 6390),
+    (1, 5000, 3, 64, 5999),
+])
+def test_workspace_bytes_follow_the_plan(shape):
+    import dit_long_sequence_gb300 as dl
+    B, Nq, H, D, kvl = shape
+    assert dl.attn_fwd_workspace_bytes(B, Nq, H, D, kvl) == _expected_bytes(B, Nq, H, D, kvl)
+
+
+def test_plan_on_a_152_sm_gb300():
+    if _sms() != 152:
+        pytest.skip("plan figures for 152 SMs")
+    assert _plan(1, 24576, 32, 24200) == (4, 3040)      # 3,072 items: 32 left over, split 4 ways
+    assert _plan(2, 44160, 16, 44160) == (2, 5472)      # 5,536 items: 64 left over, split 2 ways
+    assert _plan(2, 75600, 40, 75600) == (2, 23560)     # 120 left over, split 2 ways
+
+
+def _ws_call(q, k, v, kvl, out_dtype=torch.float32, workspace="auto"):
+    import dit_long_sequence_gb300 as dl
+    if workspace == "auto":
+        return dl.attn_fwd_ws(q, k, v, key_valid_len=kvl, out_dtype=out_dtype)
+    return dl.attn_fwd_ws(q, k, v, key_valid_len=kvl, out_dtype=out_dtype, workspace=workspace)
+
+
+@pytest.mark.parametrize("B,Nq,Nkv,H,D,kvl,f_152,seed", [
+    (1, 8192, 8192, 2, 128, 8000, 2, 21),     # 64 items, all split in two; ragged last key tile
+    (1, 2048, 16384, 2, 128, None, 8, 22),    # 16 items split 8 ways, 16 tiles per piece
+    (1, 6400, 6400, 2, 128, 6390, 3, 23),     # 50 tiles in 3 uneven ranges (16, 17, 17)
+    (1, 5000, 6000, 3, 64, 5999, 2, 24),      # D = 64, ragged query block (5000 = 19*256 + 136)
+])
+def test_split_matches_oracle_whole(B, Nq, Nkv, H, D, kvl, f_152, seed):
+    import dit_long_sequence_gb300 as dl
+    q, k, v, _ = wl.make_qkv(B, Nq, H, D, seed, device=_dev(), Nkv=Nkv)
+    kv = Nkv if kvl is None else kvl
+    f, first = _plan(B, Nq, H, kv)
+    if _sms() == 152:
+        assert f == f_152 and first == 0
+    assert dl.attn_fwd_workspace_bytes(B, Nq, H, D, kv) > 0
+    O, L = _ws_call(q, k, v, kvl)
+    Ob, Lb = _ws_call(q, k, v, kvl, out_dtype=torch.bfloat16)
+    O1, L1 = dl.attn_fwd(q, k, v, key_valid_len=kvl)
+    torch.cuda.synchronize()
+    Or, Lr = parity.oracle_full(q, k, v, key_valid_len=kvl)
+    parity.compare(O.double().cpu().numpy(), L.double().cpu().numpy(), Or, Lr, head_axes=(0, 2))
+    parity.compare(Ob.double().cpu().numpy(), Lb.double().cpu().numpy(), Or, Lr, head_axes=(0, 2))
+    assert torch.equal(L, Lb)
+    # against the single pass: P's bf16 rounding (O), fp32 rounding (LSE)
+    assert (O - O1).abs().max().item() <= SPLIT_VS_SINGLE_O
+    assert (L - L1).abs().max().item() <= SPLIT_VS_SINGLE_LSE
+    rc, info = dl.check_watchdog()
+    assert rc == 0, info
+
+
+def test_unsplit_items_bit_identical_and_null_workspace_is_plain():
+    import dit_long_sequence_gb300 as dl
+    from dit_long_sequence_gb300 import binding
+    w = wl.WORKLOADS["ltx2_padded"]
+    q, k, v, _ = wl.make_workload_inputs(w, device=_dev())
+    O, L = dl.attn_fwd_ws(q, k, v, key_valid_len=w.key_valid_len)
+    O1, L1 = dl.attn_fwd(q, k, v, key_valid_len=w.key_valid_len)
+    # NULL workspace through the C ABI: the plain kernel, bit for bit
+    O0 = torch.empty_like(O1)
+    L0 = torch.empty_like(L1)
+    st = binding.AttnStrides(binding.Strides4(*q.stride()), binding.Strides4(*k.stride()),
+                             binding.Strides4(*v.stride()), binding.Strides4(*O0.stride()))
+    rc = binding.raw().dit_attn_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(st), w.B, w.N, w.N,
+                                       w.H, w.D, w.key_valid_len, w.scale, O0.data_ptr(), binding.DIT_F32,
+                                       L0.data_ptr(), None, 0, torch.cuda.current_stream().cuda_stream)
+    assert rc == binding.DIT_OK
+    torch.cuda.synchronize()
+    assert torch.equal(O0, O1) and torch.equal(L0, L1)
+    split = torch.as_tensor(_split_rows_mask(w.B, w.N, w.H, w.kv_len), device=_dev())   # [B, H, N]
+    if not split.any():
+        pytest.skip("no split on this GPU for this shape")
+    so = split.permute(0, 2, 1)                                                        # [B, N, H]
+    assert torch.equal(O[~so], O1[~so]) and torch.equal(L[~split], L1[~split])
+    assert (O[so] - O1[so]).abs().max().item() <= SPLIT_VS_SINGLE_O
+    assert (L[split] - L1[split]).abs().max().item() <= SPLIT_VS_SINGLE_LSE
+
+
+def test_short_workspace_refused_before_enqueue():
+    import dit_long_sequence_gb300 as dl
+    B, N, H, D = 1, 8192, 2, 128
+    q, k, v, _ = wl.make_qkv(B, N, H, D, 25, device=_dev())
+    need = dl.attn_fwd_workspace_bytes(B, N, H, D, N)
+    assert need > 0
+    ws = torch.empty(need - 16, dtype=torch.uint8, device=_dev())
+    out = torch.full((B, N, H, D), float("nan"), device=_dev())
+    lse = torch.full((B, H, N), float("nan"), device=_dev())
+    with pytest.raises(dl.DitError) as e:
+        dl.attn_fwd_ws(q, k, v, out=out, lse=lse, workspace=ws)
+    assert e.value.status == 1        # DIT_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.isnan(out).all() and torch.isnan(lse).all()
+
+
+def test_ltx_workload_sampled_rows_through_the_split():
+    """The benchmark's call on the LTX-2-shaped workload: sampled rows of every
+    head, with extra rows drawn from the split items."""
+    import dit_long_sequence_gb300 as dl
+    w = wl.WORKLOADS["ltx2_padded"]
+    q, k, v, _ = wl.make_workload_inputs(w, device=_dev())
+    O, L = dl.attn_fwd_ws(q, k, v, key_valid_len=w.key_valid_len)
+    torch.cuda.synchronize()
+    f, first = _plan(w.B, w.N, w.H, w.kv_len)
+    nqb = (w.N + 255) // 256
+    must = [w.key_valid_len - 1, w.key_valid_len, w.N - 1]
+    if f > 1:
+        # rows of the first split item and of the piece boundaries' neighbourhood
+        qb0 = first % nqb
+        must += [qb0 * 256, qb0 * 256 + 255, qb0 * 256 + 128]
+    rows = wl.sample_rows(w.B, w.H, w.N, 1024, seed=w.seed, must=must)
+    Og, Lg = parity.gather_rows(O, L, rows)
+    Or, Lr = parity.oracle_rows(q, k, v, rows, key_valid_len=w.key_valid_len)
+    parity.compare(Og, Lg, Or, Lr, head_axes=(0, 1))
+    if f > 1:
+        split = _split_rows_mask(w.B, w.N, w.H, w.kv_len)
+        hit = split[np.arange(w.B)[:, None, None], np.arange(w.H)[None, :, None], rows]
+        assert hit.sum() >= 256       # the split rows are well represented in the sample
