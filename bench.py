@@ -217,16 +217,14 @@ class Step:
             self.l_parts = torch.empty((n, B, H, N), dtype=torch.float32, device=dev)
         self.out = torch.empty((B, N, H, D), dtype=torch.float32, device=dev)
         self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        # bf16 attention calls get the tail-split workspace (none when the plan has no split)
-        self.ws = None
-        if not w.fp8:
-            kvl_call = w.N // w.kv_chunks if self.mode == "chunked+merge" else w.kv_len
-            nb = dl.attn_fwd_workspace_bytes(B, N, H, D, kvl_call)
-            self.ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
+        # attention calls get the tail-split workspace (none when the plan has no split)
+        kvl_call = w.N // w.kv_chunks if self.mode == "chunked+merge" else w.kv_len
+        nb = dl.attn_fwd_workspace_bytes(B, N, H, D, kvl_call)
+        self.ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
         # attention kernel (+ the split items' piece launch and the tail merge)
         per_attn = 3 if self.ws is not None else 1
         self.launches_per_step = {"layout+attn": 1 + per_attn, "attn": per_attn,
-                                  "chunked+merge": w.kv_chunks * per_attn + 1, "cast+attn_fp8": 2}[self.mode]
+                                  "chunked+merge": w.kv_chunks * per_attn + 1, "cast+attn_fp8": 1 + per_attn}[self.mode]
         self.attn_events = []
 
     def qkv_of(self, inputs):
@@ -273,7 +271,8 @@ class Step:
                 dl.attn_fwd_ws(q, k[:, c * cl:(c + 1) * cl], v[:, c * cl:(c + 1) * cl],
                                out=self.o_parts[c], lse=self.l_parts[c], workspace=self.ws, stream=stream)
         elif self.mode == "cast+attn_fp8":
-            dl.attn_fwd_fp8(q, k, v, self.descales, key_valid_len=w.key_valid_len, out=out, lse=lse, stream=stream)
+            dl.attn_fwd_fp8_ws(q, k, v, self.descales, key_valid_len=w.key_valid_len, out=out, lse=lse,
+                               workspace=self.ws, stream=stream)
         else:
             dl.attn_fwd_ws(q, k, v, key_valid_len=w.key_valid_len, out=out, lse=lse, workspace=self.ws,
                            stream=stream)
@@ -615,16 +614,16 @@ def main(argv=None):
     traffic = profiled_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": "attn_fwd_fp8_kernel<false>" if w.fp8 else "attn_fwd_kernel<128,false,false,false>",
+                "kernel": "attn_fwd_fp8_kernel<false,false>" if w.fp8 else "attn_fwd_kernel<128,false,false,false,false>",
                 "peak_kind": (f"{peak_kind} dense bf16 burst x 2 (nominal fp8/bf16 ratio)" if w.fp8
                               else f"{peak_kind} dense bf16 burst"),
                 "flops_per_launch": per_launch_flops, "ms_per_launch": attn_ms}
-    if not w.fp8:
-        ws_bytes = 0 if step.ws is None else step.ws.numel()
-        roofline["timed"] = ("the dit_attn_fwd_ws call: attn_fwd_kernel" +
-                             (" (whole items and the split items' pieces) and attn_tail_merge_kernel" if ws_bytes
-                              else " (no tail split for this shape)"))
-        roofline["tail_split_workspace_bytes"] = ws_bytes
+    ws_bytes = 0 if step.ws is None else step.ws.numel()
+    call, kern = ("dit_attn_fwd_fp8_ws", "attn_fwd_fp8_kernel") if w.fp8 else ("dit_attn_fwd_ws", "attn_fwd_kernel")
+    roofline["timed"] = (f"the {call} call: {kern}" +
+                         (" (whole items and the split items' pieces) and attn_tail_merge_kernel" if ws_bytes
+                          else " (no tail split for this shape)"))
+    roofline["tail_split_workspace_bytes"] = ws_bytes
 
     # ---------------- secondary HBM-bound kernels
     extra = {}

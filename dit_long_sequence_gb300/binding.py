@@ -60,6 +60,9 @@ _lib.dit_attn_masked_workspace_bytes.argtypes = [_i, _i, _i]
 _lib.dit_attn_fwd_fp8.restype = _i
 _lib.dit_attn_fwd_fp8.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f, _f, _f, _f,
                                   _vp, _i, _vp, _vp]
+_lib.dit_attn_fwd_fp8_ws.restype = _i
+_lib.dit_attn_fwd_fp8_ws.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f, _f, _f,
+                                     _f, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]
 _lib.dit_qkv_cast_fp8.restype = _i
 _lib.dit_qkv_cast_fp8.argtypes = [_vp, _i64, _i64, _i, _i, _i, _i, _f, _f, _f, _vp, _vp]
 _lib.dit_qkv_norm_rope_to_head_major.restype = _i
@@ -79,7 +82,7 @@ _lib.dit_version.restype = ctypes.c_uint32
 
 EXPORTS = ("dit_attn_fwd", "dit_attn_fwd_ws", "dit_attn_fwd_workspace_bytes", "dit_attn_fwd_masked", "dit_attn_fwd_masked_noalloc", "dit_attn_masked_workspace_bytes",
            "dit_attn_fwd_accumulate", "dit_attn_lse_merge", "dit_qkv_to_head_major",
-           "dit_qkv_norm_rope_to_head_major", "dit_qkv_cast_fp8", "dit_attn_fwd_fp8", "dit_status_string",
+           "dit_qkv_norm_rope_to_head_major", "dit_qkv_cast_fp8", "dit_attn_fwd_fp8", "dit_attn_fwd_fp8_ws", "dit_status_string",
            "dit_check_watchdog",
            "dit_watchdog_selftest", "dit_version")
 
@@ -162,7 +165,7 @@ def attn_fwd_ws(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, key_valid_
     B, Nq, Nkv, H, D, kvl, sc, out, lse, st = _attn_args(q, k, v, key_valid_len, scale, out, lse, out_dtype)
     if workspace is None:
         nbytes = attn_fwd_workspace_bytes(B, Nq, H, D, kvl)
-        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device) if nbytes else None
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc = _lib.dit_attn_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(st), B, Nq, Nkv, H, D, kvl,
@@ -402,12 +405,7 @@ def qkv_cast_fp8(qkv: torch.Tensor, scales, *, out: torch.Tensor | None = None, 
     return out
 
 
-def attn_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, descales, *, key_valid_len: int | None = None,
-                 scale: float | None = None, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-                 out_dtype: torch.dtype = torch.float32, stream=None):
-    """Attention on E4M3 codes through `dit_attn_fwd_fp8`: q, k, v [B, N, H, D]
-    uint8 / float8_e4m3fn views (e.g. of qkv_cast_fp8's output) standing for
-    q * descales[0], k * descales[1], v * descales[2].  Returns (out, lse)."""
+def _attn_fp8_args(q, k, v, descales, key_valid_len, scale, out, lse, out_dtype):
     B, Nq, H, D = q.shape
     Nkv = k.shape[1]
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -427,10 +425,42 @@ def attn_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, descales, *,
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
     st = AttnStrides(_strides4(q), _strides4(k), _strides4(v), _strides4(out))
+    return B, Nq, Nkv, H, D, kvl, sc, dq, dk, dv, out, lse, st
+
+
+def attn_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, descales, *, key_valid_len: int | None = None,
+                 scale: float | None = None, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                 out_dtype: torch.dtype = torch.float32, stream=None):
+    """Attention on E4M3 codes through `dit_attn_fwd_fp8`: q, k, v [B, N, H, D]
+    uint8 / float8_e4m3fn views (e.g. of qkv_cast_fp8's output) standing for
+    q * descales[0], k * descales[1], v * descales[2].  Returns (out, lse)."""
+    B, Nq, Nkv, H, D, kvl, sc, dq, dk, dv, out, lse, st = _attn_fp8_args(q, k, v, descales, key_valid_len, scale,
+                                                                         out, lse, out_dtype)
     rc = _lib.dit_attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(st), B, Nq, Nkv, H, D, kvl,
                                sc, dq, dk, dv, out.data_ptr(), DIT_F32 if out.dtype == torch.float32 else DIT_BF16,
                                lse.data_ptr(), _stream_ptr(stream))
     _check(rc, "dit_attn_fwd_fp8")
+    return out, lse
+
+
+def attn_fwd_fp8_ws(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, descales, *,
+                    key_valid_len: int | None = None, scale: float | None = None, out: torch.Tensor | None = None,
+                    lse: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32,
+                    workspace: torch.Tensor | None = None, stream=None):
+    """attn_fwd_fp8 through `dit_attn_fwd_fp8_ws`: the grid's last partial wave
+    split over key ranges and merged.  The workspace (a uint8 CUDA tensor of
+    attn_fwd_workspace_bytes) is allocated here unless given."""
+    B, Nq, Nkv, H, D, kvl, sc, dq, dk, dv, out, lse, st = _attn_fp8_args(q, k, v, descales, key_valid_len, scale,
+                                                                         out, lse, out_dtype)
+    if workspace is None:
+        nbytes = attn_fwd_workspace_bytes(B, Nq, H, D, kvl)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = _lib.dit_attn_fwd_fp8_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(st), B, Nq, Nkv, H, D, kvl,
+                                  sc, dq, dk, dv, out.data_ptr(), DIT_F32 if out.dtype == torch.float32 else DIT_BF16,
+                                  lse.data_ptr(), ws_ptr, ws_bytes, _stream_ptr(stream))
+    _check(rc, "dit_attn_fwd_fp8_ws")
     return out, lse
 
 

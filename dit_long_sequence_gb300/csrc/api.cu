@@ -207,7 +207,7 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
     // when the caller gave a workspace for it (plain, unmasked, overwrite only).
     const int64_t items = static_cast<int64_t>(B) * H * ((static_cast<int64_t>(Nq) + 255) / 256);
     SplitPlan split{items, 1, 0};
-    if (workspace != nullptr && !fp8 && !accumulate && mask == nullptr && any_keys) {
+    if (workspace != nullptr && !accumulate && mask == nullptr && any_keys) {
         split = plan_tail_split(items, (key_valid_len + 127) / 128, device_sm_count(dev));
         if (workspace_bytes < static_cast<size_t>(split_workspace_bytes(split, D))) return DIT_ERR_INVALID_ARG;
         if (!aligned16(workspace)) return DIT_ERR_ALIGNMENT;
@@ -267,7 +267,7 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
     const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = fp8 ? launch_attn_fwd_fp8(tq, tk, tv, a, B, out_dtype == DIT_BF16, cs)
                         : launch_attn_fwd(tq, tk, tv, a, B, D, out_dtype == DIT_BF16, accumulate, cs);
-    if (e == cudaSuccess && !fp8) e = launch_attn_tail_merge(a, D, out_dtype == DIT_BF16, cs);
+    if (e == cudaSuccess) e = launch_attn_tail_merge(a, D, out_dtype == DIT_BF16, cs);
     return e == cudaSuccess ? DIT_OK : DIT_ERR_CUDA;
 }
 
@@ -357,6 +357,15 @@ dit_status_t dit_attn_fwd_fp8(const void* q, const void* k, const void* v, const
     const float descales[3] = {descale_q, descale_k, descale_v};
     return attn_fwd_common(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, scale, out, out_dtype, lse, false,
                            stream, descales);
+}
+
+dit_status_t dit_attn_fwd_fp8_ws(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides,
+                                 int B, int Nq, int Nkv, int H, int D, int key_valid_len, float scale,
+                                 float descale_q, float descale_k, float descale_v, void* out, dit_dtype_t out_dtype,
+                                 float* lse, void* workspace, size_t workspace_bytes, dit_stream_t stream) {
+    const float descales[3] = {descale_q, descale_k, descale_v};
+    return attn_fwd_common(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, scale, out, out_dtype, lse, false,
+                           stream, descales, nullptr, workspace, workspace_bytes);
 }
 
 dit_status_t dit_qkv_cast_fp8(const void* qkv, int64_t stride_b, int64_t stride_n, int B, int N, int H, int D,

@@ -23,6 +23,10 @@
 // smallest kept values (2^-9) are ~2^-16 below the row max.  Unlike the bf16
 // kernel, this needs the tile max every tile.  The row sum l accumulates the
 // unrounded fp32 P; O = (sum P v8) * descale_v / l.
+//
+// The epilogue stages O through the idle Q buffer and stores whole 128-byte
+// lines, and the grid's last partial wave can be split over key ranges
+// (PIECE, a programmatic dependent launch), exactly as in the bf16 kernel.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -71,7 +75,9 @@ __device__ __forceinline__ float max64(const float* v) {
     return max3f(max3f(t8[0], t8[1], t8[2]), max3f(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
 }
 
-template <bool OUT_BF16>
+// PIECE: the kernel of the split items' key-range pieces (1-D grid, partials
+// to the workspace); the whole-item kernel is compiled without any of it.
+template <bool OUT_BF16, bool PIECE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
@@ -89,10 +95,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int h = blockIdx.y;
-    const int b = blockIdx.z;
-    const int q_row0 = blockIdx.x * (2 * kBM);
-    const int n_tiles = a.n_kv_tiles;
+    // Work item of this CTA: (256-row block, head, batch) = (x, y, z) for a
+    // whole item; a piece decodes its item and first key tile from its 1-D
+    // index (items counted block fastest, then head, then batch).
+    int k_begin = 0, n_tiles = a.n_kv_tiles;
+    int h, b, q_row0;
+    if constexpr (PIECE) {
+        const int slot = static_cast<int>(blockIdx.x);
+        const int piece = slot % a.split_f;
+        const int item = a.split_first + slot / a.split_f;
+        k_begin = static_cast<int>(static_cast<int64_t>(piece) * a.n_kv_tiles / a.split_f);
+        n_tiles = static_cast<int>(static_cast<int64_t>(piece + 1) * a.n_kv_tiles / a.split_f) - k_begin;
+        q_row0 = (item % a.n_qblk) * (2 * kBM);
+        h = (item / a.n_qblk) % a.H;
+        b = item / a.n_qblk / a.H;
+    } else {
+        h = blockIdx.y;
+        b = blockIdx.z;
+        q_row0 = blockIdx.x * (2 * kBM);
+        // The piece kernel (if any) may start once every CTA here has begun;
+        // the items it covers are the last in grid order and left to it.
+        if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        if (static_cast<int>(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)) >= a.split_first) return;
+    }
 
     if (threadIdx.x == 0) {
         mbar_init(bar(kQFull + 0), 1);
@@ -143,8 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
                 if (!wait_bounded(bar(kKVEmpty + slot), ph ^ 1u, wd, ROLE_LOAD, SITE_KV_EMPTY)) break;
                 mbar_arrive_expect_tx(bar(kKVFull + slot), kTile);
-                tma_load_4d(sRing + slot * kTile, (i & 1) ? &tm_v : &tm_k, bar(kKVFull + slot), 0, (i >> 1) * kBN, h,
-                            b);
+                tma_load_4d(sRing + slot * kTile, (i & 1) ? &tm_v : &tm_k, bar(kKVFull + slot), 0,
+                            (k_begin + (i >> 1)) * kBN, h, b);
                 issued = i + 1;
             }
             if (issued < total || *abort_flag) {
@@ -279,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             reg_dep(sr[1]);
             reg_dep(sr[2]);
             reg_dep(sr[3]);
-            const int valid = a.kv_len - j * kBN;   // >= 1
+            const int valid = a.kv_len - (k_begin + j) * kBN;   // >= 1
             float s[128];
 #pragma unroll
             for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
@@ -323,11 +348,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             const bool in_range = row < a.Nq;
-            const int64_t o_off = static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(row) * a.o_sn +
-                                  static_cast<int64_t>(h) * a.o_sh;
             const int64_t lse_idx = (static_cast<int64_t>(b) * a.H + h) * a.Nq + row;
             const float c_new = n_tiles > 0 ? a.o_scale / l : 0.f;
-#pragma unroll
+            // Each 32-column chunk goes through this warp's 4 KB of the Q_t buffer
+            // (idle since QK_t(last) completed): a thread writes its row, then the
+            // warp stores four rows per instruction as whole 128-byte lines.  Rows
+            // sit 128 bytes apart with the 16-byte groups XOR-swizzled by the row.
+            float4* stg = reinterpret_cast<float4*>(smem + t * kTile + wq * 4096);
+            const int k4 = lane & 7;        // 16-byte group this lane moves in the store phase
+            const int r_sub = lane >> 3;    // row within each group of four
+#pragma unroll 1
             for (int cc = 0; cc < kD / 32; ++cc) {
                 uint32_t o[32];
                 if (n_tiles > 0) {
@@ -337,28 +367,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = 0u;
                 }
-                if (in_range) {
-                    if constexpr (OUT_BF16) {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + o_off + cc * 32);
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * c_new, __uint_as_float(o[8 * v4 + 1]) * c_new);
-                            w.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * c_new, __uint_as_float(o[8 * v4 + 3]) * c_new);
-                            w.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * c_new, __uint_as_float(o[8 * v4 + 5]) * c_new);
-                            w.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * c_new, __uint_as_float(o[8 * v4 + 7]) * c_new);
-                            dst[v4] = w;
-                        }
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + o_off + cc * 32);
+                for (int v4 = 0; v4 < 8; ++v4)
+                    stg[lane * 8 + (v4 ^ (lane & 7))] =
+                        make_float4(__uint_as_float(o[4 * v4 + 0]) * c_new, __uint_as_float(o[4 * v4 + 1]) * c_new,
+                                    __uint_as_float(o[4 * v4 + 2]) * c_new, __uint_as_float(o[4 * v4 + 3]) * c_new);
+                __syncwarp();
 #pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
-                            dst[v4] = make_float4(__uint_as_float(o[4 * v4 + 0]) * c_new, __uint_as_float(o[4 * v4 + 1]) * c_new,
-                                                  __uint_as_float(o[4 * v4 + 2]) * c_new, __uint_as_float(o[4 * v4 + 3]) * c_new);
+                for (int it = 0; it < 8; ++it) {
+                    const int r = it * 4 + r_sub;                   // row within the warp's 32
+                    const float4 val = stg[r * 8 + (k4 ^ (r & 7))];
+                    const int grow = q_row0 + t * kBM + wq * 32 + r;
+                    if (PIECE && grow < a.Nq) {
+                        // a piece's fp32 partial, row-major [256][D] in its workspace slot
+                        *reinterpret_cast<float4*>(a.ws_o + (static_cast<int64_t>(blockIdx.x) * (2 * kBM) + (grow - q_row0)) * kD +
+                                                   cc * 32 + 4 * k4) = val;
+                    } else if (grow < a.Nq) {
+                        const int64_t off = static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(grow) * a.o_sn +
+                                            static_cast<int64_t>(h) * a.o_sh + cc * 32 + 4 * k4;
+                        if constexpr (OUT_BF16)
+                            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + off) =
+                                make_uint2(pack_bf16x2(val.x, val.y), pack_bf16x2(val.z, val.w));
+                        else
+                            *reinterpret_cast<float4*>(static_cast<float*>(a.out) + off) = val;
                     }
                 }
+                __syncwarp();
             }
-            if (in_range) a.lse[lse_idx] = n_tiles > 0 ? (m - kPOffset + log2f(l)) * kLn2 : -INFINITY;
+            const float lse_out = n_tiles > 0 ? (m - kPOffset + log2f(l)) * kLn2 : -INFINITY;
+            if (in_range) {
+                if (PIECE)
+                    a.ws_lse[static_cast<int64_t>(blockIdx.x) * (2 * kBM) + (row - q_row0)] = lse_out;
+                else
+                    a.lse[lse_idx] = lse_out;
+            }
         }
     }
 
@@ -368,6 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    // A piece completes only after the whole-item grid it was launched beside
+    // (whose outputs are the stream's too); by then that grid has no CTA left
+    // to schedule, so the wait holds nothing back.
+    if constexpr (PIECE) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <bool BF16>
@@ -378,7 +424,24 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     if (e != cudaSuccess) return e;
     const dim3 grid((args.Nq + 2 * kBM - 1) / (2 * kBM), args.H, B);
     kern<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, args);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess || args.n_split_ctas == 0) return e;
+    // The split items' pieces: a programmatic dependent launch, so that its
+    // CTAs take SMs as the last whole items drain instead of after the grid.
+    auto piece = attn_fwd_fp8_kernel<BF16, true>;
+    e = cudaFuncSetAttribute(piece, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(args.n_split_ctas));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, piece, tq, tk, tv, args);
 }
 
 }  // namespace

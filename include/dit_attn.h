@@ -17,7 +17,8 @@
  *   dit_qkv_norm_rope_to_head_major  the same split with Q/K RMSNorm and
  *                          rotary embedding fused in (V copied).
  *   dit_qkv_cast_fp8       one-pass scaled bf16 -> E4M3 cast of that stacked
- *                          buffer, and dit_attn_fwd_fp8, the attention that
+ *                          buffer, and dit_attn_fwd_fp8 (dit_attn_fwd_fp8_ws
+ *                          with the balancing workspace), the attention that
  *                          reads its output in place.
  *
  * Conventions shared by every entry point
@@ -140,7 +141,8 @@ dit_status_t dit_attn_fwd_ws(const void *q, const void *k, const void *v,
                              dit_stream_t stream);
 
 /*
- * dit_attn_fwd_workspace_bytes -- workspace bytes dit_attn_fwd_ws uses for this
+ * dit_attn_fwd_workspace_bytes -- workspace bytes dit_attn_fwd_ws (and
+ * dit_attn_fwd_fp8_ws, D = 128) uses for this
  * shape on the CURRENT device (the plan depends on its SM count): the split
  * pieces' fp32 partial O (256 x D per piece) and LSE (256 per piece).  0 when
  * no split helps (the item count is a multiple of the SM count, the keys are
@@ -386,6 +388,33 @@ dit_status_t dit_attn_fwd_fp8(const void *q, const void *k, const void *v,
                               float descale_q, float descale_k, float descale_v,
                               void *out, dit_dtype_t out_dtype, float *lse,
                               dit_stream_t stream);
+
+/*
+ * dit_attn_fwd_fp8_ws -- dit_attn_fwd_fp8 with the grid-balancing workspace of
+ * dit_attn_fwd_ws: the work items of the last partial wave run as key-range
+ * pieces (a programmatic dependent launch) beside the last whole items, and
+ * their normalised partial (O, LSE) pairs are combined with the exact merge of
+ * "Scaling Video Generation Across NVL72 rack with TensorRT-LLM", "Ring
+ * Attention", paragraph "Online-softmax merge".  The pages have no counterpart
+ * for the scheduling.
+ *
+ * workspace  NULL (then exactly dit_attn_fwd_fp8), or device memory of at least
+ *        dit_attn_fwd_workspace_bytes(B, Nq, H, D, key_valid_len) bytes (the
+ *        same plan as the bf16 call), 16-byte aligned, owned by the caller and
+ *        not used by anything else until the stream has passed the call.  A
+ *        smaller non-zero size is DIT_ERR_INVALID_ARG.
+ * Other arguments and results as dit_attn_fwd_fp8.  Items that are not split
+ * are bit-identical to dit_attn_fwd_fp8's; split items differ by the E4M3
+ * rounding of P (each piece rounds against its own running max).
+ */
+dit_status_t dit_attn_fwd_fp8_ws(const void *q, const void *k, const void *v,
+                                 const dit_attn_strides_t *strides,
+                                 int B, int Nq, int Nkv, int H, int D,
+                                 int key_valid_len, float scale,
+                                 float descale_q, float descale_k, float descale_v,
+                                 void *out, dit_dtype_t out_dtype, float *lse,
+                                 void *workspace, size_t workspace_bytes,
+                                 dit_stream_t stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *dit_status_string(dit_status_t s);

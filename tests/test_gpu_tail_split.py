@@ -198,3 +198,97 @@ def test_ltx_workload_sampled_rows_through_the_split():
         split = _split_rows_mask(w.B, w.N, w.H, w.kv_len)
         hit = split[np.arange(w.B)[:, None, None], np.arange(w.H)[None, :, None], rows]
         assert hit.sum() >= 256       # the split rows are well represented in the sample
+
+
+# ------------------------------------------------------------------ FP8 path
+
+def _fp8_vmax(v8) -> float:
+    import oracle
+    codes = np.asarray(parity.host_u8(v8))
+    return float(oracle.e4m3_decode(np.array([int((codes & 0x7F).max())], dtype=np.uint8))[0])
+
+
+@pytest.mark.parametrize("B,N,H,kvl,out_dtype,f_152,seed", [
+    (1, 8192, 2, 8000, torch.float32, 2, 31),      # 64 items, all split in two, ragged last key tile
+    (1, 2048, 2, 2000, torch.bfloat16, 0, 32),     # 16 items, 16 tiles: too few keys, no split
+])
+def test_fp8_split_matches_oracle_whole(B, N, H, kvl, out_dtype, f_152, seed):
+    import dit_long_sequence_gb300 as dl
+    import oracle
+    D = 128
+    qkv8 = wl.randn_e4m3((B, N, 3, H, D), seed, 64.0, _dev())
+    q8, k8, v8 = dl.split_stacked_fp8(qkv8)
+    desc = (1 / 64, 1 / 64, 1 / 64)
+    f, first = _plan(B, N, H, kvl)
+    if _sms() == 152 and f_152:
+        assert f == f_152 and first == 0
+    O, L = dl.attn_fwd_fp8_ws(q8, k8, v8, desc, key_valid_len=kvl, out_dtype=out_dtype)
+    O1, L1 = dl.attn_fwd_fp8(q8, k8, v8, desc, key_valid_len=kvl, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    Oref, Lref = oracle.attn_fp8(*(parity.host_u8(t) for t in (q8, k8, v8)), scale=D ** -0.5, descale_q=desc[0],
+                                 descale_k=desc[1], descale_v=desc[2], key_valid_len=kvl)
+    vmax = _fp8_vmax(v8) * desc[2]
+    parity.compare_fp8(O.double().permute(0, 2, 1, 3).cpu().numpy(), L.double().cpu().numpy(),
+                       Oref.transpose(0, 2, 1, 3), Lref, vmax)
+    # against the single pass: each is within the E4M3 bound of the oracle
+    assert (O.float() - O1.float()).abs().max().item() <= 2 * (2.0 ** -4 * vmax + 1e-3)
+    assert (L - L1).abs().max().item() <= SPLIT_VS_SINGLE_LSE
+    if f == 1:
+        assert torch.equal(O, O1) and torch.equal(L, L1)
+
+
+def test_fp8_split_8_ways_matches_oracle():
+    import dit_long_sequence_gb300 as dl
+    import oracle
+    B, N, Nkv, H, D = 1, 2048, 16384, 2, 128
+    q8 = wl.randn_e4m3((B, N, H, D), 33, 64.0, _dev())
+    kv8 = wl.randn_e4m3((B, Nkv, 2, H, D), 34, 64.0, _dev())
+    k8, v8 = kv8[:, :, 0], kv8[:, :, 1]
+    desc = (1 / 64, 1 / 64, 1 / 64)
+    if _sms() == 152:
+        assert _plan(B, N, H, Nkv) == (8, 0)
+    O, L = dl.attn_fwd_fp8_ws(q8, k8, v8, desc)
+    torch.cuda.synchronize()
+    Oref, Lref = oracle.attn_fp8(*(parity.host_u8(t) for t in (q8, k8, v8)), scale=D ** -0.5, descale_q=desc[0],
+                                 descale_k=desc[1], descale_v=desc[2])
+    parity.compare_fp8(O.double().permute(0, 2, 1, 3).cpu().numpy(), L.double().cpu().numpy(),
+                       Oref.transpose(0, 2, 1, 3), Lref, _fp8_vmax(v8) * desc[2])
+
+
+def test_fp8_ltx_workload_through_the_split():
+    """The benchmark's FP8 call on the LTX-2-shaped workload: unsplit items
+    bit-identical to dit_attn_fwd_fp8, a NULL workspace exactly that call, and
+    sampled rows of the split items (and every head) against the oracle."""
+    import dit_long_sequence_gb300 as dl
+    import oracle
+    from dit_long_sequence_gb300 import binding
+    w = wl.WORKLOADS["ltx2_padded_fp8"]
+    buf = wl.randn_bf16((w.B, w.N, 3, w.H, w.D), w.seed, _dev())
+    qkv8 = dl.qkv_cast_fp8(buf, wl.FP8_SCALES)
+    q8, k8, v8 = dl.split_stacked_fp8(qkv8)
+    desc = tuple(1.0 / s for s in wl.FP8_SCALES)
+    O, L = dl.attn_fwd_fp8_ws(q8, k8, v8, desc, key_valid_len=w.key_valid_len)
+    O1, L1 = dl.attn_fwd_fp8(q8, k8, v8, desc, key_valid_len=w.key_valid_len)
+    O0, L0 = torch.empty_like(O1), torch.empty_like(L1)
+    st = binding.AttnStrides(binding.Strides4(*q8.stride()), binding.Strides4(*k8.stride()),
+                             binding.Strides4(*v8.stride()), binding.Strides4(*O0.stride()))
+    rc = binding.raw().dit_attn_fwd_fp8_ws(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), ctypes.byref(st), w.B, w.N,
+                                           w.N, w.H, w.D, w.key_valid_len, w.scale, *desc, O0.data_ptr(),
+                                           binding.DIT_F32, L0.data_ptr(), None, 0,
+                                           torch.cuda.current_stream().cuda_stream)
+    assert rc == binding.DIT_OK
+    torch.cuda.synchronize()
+    assert torch.equal(O0, O1) and torch.equal(L0, L1)
+    f, first = _plan(w.B, w.N, w.H, w.kv_len)
+    split = torch.as_tensor(_split_rows_mask(w.B, w.N, w.H, w.kv_len), device=_dev())
+    so = split.permute(0, 2, 1)
+    assert torch.equal(O[~so], O1[~so]) and torch.equal(L[~split], L1[~split])
+    must = [w.key_valid_len - 1, w.key_valid_len, w.N - 1]
+    if f > 1:
+        qb0 = first % ((w.N + 255) // 256)
+        must += [qb0 * 256, qb0 * 256 + 255, qb0 * 256 + 128]
+    rows = wl.sample_rows(w.B, w.H, w.N, 512, seed=w.seed, must=must)
+    Og, Lg = parity.gather_rows(O, L, rows)
+    Oref, Lref = oracle.attn_fp8(*(parity.host_u8(t) for t in (q8, k8, v8)), scale=w.scale, descale_q=desc[0],
+                                 descale_k=desc[1], descale_v=desc[2], key_valid_len=w.key_valid_len, rows=rows)
+    parity.compare_fp8(Og, Lg, Oref, Lref, _fp8_vmax(v8) * desc[2])
