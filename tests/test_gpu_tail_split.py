@@ -292,3 +292,40 @@ def test_fp8_ltx_workload_through_the_split():
     Oref, Lref = oracle.attn_fp8(*(parity.host_u8(t) for t in (q8, k8, v8)), scale=w.scale, descale_q=desc[0],
                                  descale_k=desc[1], descale_v=desc[2], key_valid_len=w.key_valid_len, rows=rows)
     parity.compare_fp8(Og, Lg, Oref, Lref, _fp8_vmax(v8) * desc[2])
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_stream_order_covers_the_whole_call(fp8):
+    """Work queued on the stream right after the call sees every output row:
+    the piece launch completes only after the whole-item grid beside it, so a
+    reader (a copy on the same side stream, with no host sync in between) never
+    observes rows the whole-item grid has not written yet."""
+    import dit_long_sequence_gb300 as dl
+    w = wl.WORKLOADS["ltx2_padded"]
+    side = torch.cuda.Stream()
+    if fp8:
+        qkv8 = wl.randn_e4m3((w.B, w.N, 3, w.H, w.D), w.seed, 64.0, _dev())
+        q, k, v = dl.split_stacked_fp8(qkv8)
+        d = (1 / 64, 1 / 64, 1 / 64)
+        ref, ref_l = dl.attn_fwd_fp8(q, k, v, d, key_valid_len=w.key_valid_len)
+        call = lambda o, l, s: dl.attn_fwd_fp8_ws(q, k, v, d, key_valid_len=w.key_valid_len, out=o, lse=l, stream=s)
+    else:
+        q, k, v, _ = wl.make_workload_inputs(w, device=_dev())
+        ref, ref_l = dl.attn_fwd(q, k, v, key_valid_len=w.key_valid_len)
+        call = lambda o, l, s: dl.attn_fwd_ws(q, k, v, key_valid_len=w.key_valid_len, out=o, lse=l, stream=s)
+    torch.cuda.synchronize()
+    split = torch.as_tensor(_split_rows_mask(w.B, w.N, w.H, w.kv_len), device=_dev())
+    out = torch.empty_like(ref)
+    lse = torch.empty_like(ref_l)
+    side.wait_stream(torch.cuda.current_stream())
+    for _ in range(4):
+        with torch.cuda.stream(side):
+            out.fill_(float("nan"))
+            lse.fill_(float("nan"))
+            call(out, lse, side)
+            seen_o = out.clone()          # queued behind the call, no host sync in between
+            seen_l = lse.clone()
+        torch.cuda.synchronize()
+        assert not torch.isnan(seen_o).any() and not torch.isnan(seen_l).any()
+        so = split.permute(0, 2, 1)
+        assert torch.equal(seen_o[~so], ref[~so]) and torch.equal(seen_l[~split], ref_l[~split])
