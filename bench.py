@@ -86,11 +86,14 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    _count = 0   # one file per sampler in this process
+
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.t0 = self.t1 = None
-        self.path = os.path.join(tempfile.gettempdir(), f"dit_bench_clocks_{os.getpid()}.csv")
+        ClockSampler._count += 1
+        self.path = os.path.join(tempfile.gettempdir(), f"dit_bench_clocks_{os.getpid()}_{ClockSampler._count}.csv")
 
     def __enter__(self):
         try:
@@ -715,6 +718,9 @@ def run_e2e(step, args, world):
     torch.cuda.synchronize()
     barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # No nvidia-smi sampling in this window: its polling slowed this three-stream
+    # pipeline (9.35 vs 6.71 ms per step over 40 LTX-2 steps), while the
+    # single-stream device window above shows no such effect.
     pipeline(args.steps, a, b)
     torch.cuda.synchronize()
     barrier()
