@@ -298,6 +298,13 @@ class Step:
         per = self.w.kv_chunks if self.mode == "chunked+merge" else 1
         return statistics.mean(times) / per if times else float("nan")
 
+    def attn_ms_median(self):
+        import torch
+        torch.cuda.synchronize()
+        times = [a.elapsed_time(b) for a, b in self.attn_events]
+        per = self.w.kv_chunks if self.mode == "chunked+merge" else 1
+        return statistics.median(times) / per if times else float("nan")
+
 
 def time_merge_kernel(dev, B, N, H, D, n_chunks=9, reps=5, interleaved=True):
     """HBM roofline of dit_attn_lse_merge on ring-style partials of this shape
@@ -620,7 +627,8 @@ def main(argv=None):
                 "kernel": "attn_fwd_fp8_kernel<false,false>" if w.fp8 else "attn_fwd_kernel<128,false,false,false,false>",
                 "peak_kind": (f"{peak_kind} dense bf16 burst x 2 (nominal fp8/bf16 ratio)" if w.fp8
                               else f"{peak_kind} dense bf16 burst"),
-                "flops_per_launch": per_launch_flops, "ms_per_launch": attn_ms}
+                "flops_per_launch": per_launch_flops, "ms_per_launch": attn_ms,
+                "ms_per_launch_median": step.attn_ms_median()}
     ws_bytes = 0 if step.ws is None else step.ws.numel()
     call, kern = ("dit_attn_fwd_fp8_ws", "attn_fwd_fp8_kernel") if w.fp8 else ("dit_attn_fwd_ws", "attn_fwd_kernel")
     roofline["timed"] = (f"the {call} call: {kern}" +

@@ -329,3 +329,22 @@ def test_stream_order_covers_the_whole_call(fp8):
         assert not torch.isnan(seen_o).any() and not torch.isnan(seen_l).any()
         so = split.permute(0, 2, 1)
         assert torch.equal(seen_o[~so], ref[~so]) and torch.equal(seen_l[~split], ref_l[~split])
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_split_reruns_are_bit_identical(fp8):
+    """The pieces' partials are combined in a fixed order, so the split call is
+    deterministic run to run, like the plain kernel."""
+    import dit_long_sequence_gb300 as dl
+    B, N, H, D, kvl = 1, 8192, 2, 128, 8000
+    if fp8:
+        q, k, v = dl.split_stacked_fp8(wl.randn_e4m3((B, N, 3, H, D), 41, 64.0, _dev()))
+        run = lambda: dl.attn_fwd_fp8_ws(q, k, v, (1 / 64, 1 / 64, 1 / 64), key_valid_len=kvl)
+    else:
+        q, k, v, _ = wl.make_qkv(B, N, H, D, 41, device=_dev())
+        run = lambda: dl.attn_fwd_ws(q, k, v, key_valid_len=kvl)
+    O1, L1 = run()
+    O2, L2 = run()
+    torch.cuda.synchronize()
+    assert dl.attn_fwd_workspace_bytes(B, N, H, D, kvl) > 0
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
