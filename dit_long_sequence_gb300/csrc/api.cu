@@ -173,6 +173,10 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
     }
     if (D != 64 && D != 128) return DIT_ERR_UNSUPPORTED;
     if (B > 65535 || H > 65535) return DIT_ERR_UNSUPPORTED;
+    // The work items (b, h, 256-row block) are counted in 32-bit ints on the
+    // device (grid order, the split boundary).
+    if (static_cast<int64_t>(B) * H * ((static_cast<int64_t>(Nq) + 255) / 256) > 0x7fffffffLL)
+        return DIT_ERR_UNSUPPORTED;
     if (B == 0 || Nq == 0 || H == 0) return DIT_OK;
     if (out == nullptr || lse == nullptr) return DIT_ERR_INVALID_ARG;
     const bool any_keys = key_valid_len > 0;

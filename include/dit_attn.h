@@ -91,7 +91,9 @@ typedef struct {
  * strides  s.q.d, s.k.d, s.v.d, s.o.d must be 1.  The b, n, h strides of q/k/v
  *          must be positive multiples of 8 elements (16 bytes); those of o
  *          multiples of 16 bytes of out_dtype.  Base pointers 16-byte aligned.
- * B, Nq, Nkv, H  >= 0 (a zero size is a no-op); D in {64, 128}.
+ * B, Nq, Nkv, H  >= 0 (a zero size is a no-op); D in {64, 128}.  B and H at
+ *          most 65,535 and B * H * ceil(Nq / 256) below 2^31, else
+ *          DIT_ERR_UNSUPPORTED (the same limits hold for every attention call).
  * key_valid_len  keys j >= key_valid_len are masked out; 0 <= key_valid_len <= Nkv.
  *          Masked keys are never read, so pad rows may hold any bits.
  *          key_valid_len == 0 yields O = 0 and LSE = -inf for every row.

@@ -230,6 +230,10 @@ def test_attn_fwd_ws_argument_checks(lib):
     assert call(out=None) == lib.DIT_ERR_INVALID_ARG
     assert call(out=FAKE + 4) == lib.DIT_ERR_ALIGNMENT
     assert call(B=0) == lib.DIT_OK
+    # more than 2^31 - 1 work items (b, h, 256-row block): refused before any device call
+    big = f(FAKE, FAKE, FAKE, ctypes.byref(st), 65535, 256 * 1000, 8, 65535, 128, 8, 0.088, FAKE, lib.DIT_F32,
+            FAKE, None, 0, None)
+    assert big == lib.DIT_ERR_UNSUPPORTED
     wsb = lib.raw().dit_attn_fwd_workspace_bytes
     assert wsb(1, 24576, 32, 96, 24200) == 0          # unsupported D
     assert wsb(0, 24576, 32, 128, 24200) == 0 and wsb(1, 24576, 32, 128, 0) == 0
