@@ -11,7 +11,9 @@ LSE over the head-major views (dit_attn_fwd_ws: dit_attn_fwd with a workspace
 that splits the grid's last partial wave over key ranges, plus the small
 kernel that merges those pieces).  Other workloads: cosmos3_nano
 (attention straight on strided views of the fused buffer), wan22_a14b
-(separate Q/K/V), ring9 (9 key chunks, 9 attention calls + dit_attn_lse_merge).
+(separate Q/K/V), ring9 (9 key chunks, 9 attention calls + dit_attn_lse_merge),
+ltx2_padded_fp8 / wan22_a14b_fp8 (one-pass E4M3 cast of the stacked buffer,
+then dit_attn_fwd_fp8_ws).
 
 Printed (rank 0, one JSON line): value = algorithmic FLOPs of all ranks / max
 over ranks of the device time of K steps; e2e = the same metric through the
