@@ -149,12 +149,22 @@ def test_watchdog_clean_after_runs():
 
 
 def _sampled_check(w, rows_per_head=1024):
+    """The workload in the benchmark's launch configuration: dit_attn_fwd_ws,
+    whose last partial wave of work items runs as key-range pieces; the sample
+    includes the first split item's edge rows."""
+    import dit_long_sequence_gb300 as dl
     q, k, v, buf = wl.make_workload_inputs(w, device=_dev())
-    O, L = _attn(q, k, v, key_valid_len=w.key_valid_len)
+    O, L = dl.attn_fwd_ws(q, k, v, key_valid_len=w.key_valid_len)
     torch.cuda.synchronize()
     must = [w.N - 80, w.N - 1]
     if w.key_valid_len is not None:
         must += [w.key_valid_len - 1, w.key_valid_len, w.N - 1]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nqb = (w.N + 255) // 256
+    tail = (w.B * w.H * nqb) % sms
+    if tail:
+        qb0 = (w.B * w.H * nqb - tail) % nqb      # block of the first split item
+        must += [qb0 * 256, qb0 * 256 + 127, qb0 * 256 + 128, min(w.N - 1, qb0 * 256 + 255)]
     rows = wl.sample_rows(w.B, w.H, w.N, rows_per_head, seed=w.seed, must=must)
     Og, Lg = parity.gather_rows(O, L, rows)
     Or, Lr = parity.oracle_rows(q, k, v, rows, key_valid_len=w.key_valid_len)

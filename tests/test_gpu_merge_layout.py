@@ -92,7 +92,9 @@ def test_chunked_attention_merge_equals_single_pass():
 
 
 def test_ring9_workload_chunked_vs_oracle_and_single_pass():
-    # the attention writes each chunk's O straight into a per-row interleaved
+    # the benchmark's ring-9 step: 9 chunk calls through dit_attn_fwd_ws (each
+    # chunk's last partial wave of work items split over key ranges); the
+    # attention writes each chunk's O straight into a per-row interleaved
     # [B, N, H, n, D] buffer through its output strides; the merge reads it back
     w = wl.WORKLOADS["ring9"]
     q, k, v, _ = wl.make_workload_inputs(w, device=_dev())
@@ -101,8 +103,8 @@ def test_ring9_workload_chunked_vs_oracle_and_single_pass():
     o_buf = torch.empty(w.B, w.N, w.H, n, w.D, device=_dev())
     l_parts = torch.empty(n, w.B, w.H, w.N, device=_dev())
     for c in range(n):
-        _dl().attn_fwd(q, k[:, c * cl:(c + 1) * cl], v[:, c * cl:(c + 1) * cl], out=o_buf[:, :, :, c],
-                       lse=l_parts[c])
+        _dl().attn_fwd_ws(q, k[:, c * cl:(c + 1) * cl], v[:, c * cl:(c + 1) * cl], out=o_buf[:, :, :, c],
+                          lse=l_parts[c])
     O, L = _dl().lse_merge(o_buf.permute(3, 0, 1, 2, 4), l_parts)
     del o_buf, l_parts
     O1, L1 = _dl().attn_fwd(q, k, v)
