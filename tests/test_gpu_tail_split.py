@@ -210,6 +210,8 @@ def _fp8_vmax(v8) -> float:
 
 @pytest.mark.parametrize("B,N,H,kvl,out_dtype,f_152,seed", [
     (1, 8192, 2, 8000, torch.float32, 2, 31),      # 64 items, all split in two, ragged last key tile
+    (1, 8192, 2, 8000, torch.bfloat16, 2, 35),     # the same split with bf16 output
+    (2, 4500, 3, 4400, torch.float32, 2, 36),      # B = 2, ragged query blocks: 108 items split in two
     (1, 2048, 2, 2000, torch.bfloat16, 0, 32),     # 16 items, 16 tiles: too few keys, no split
 ])
 def test_fp8_split_matches_oracle_whole(B, N, H, kvl, out_dtype, f_152, seed):
