@@ -108,6 +108,7 @@ def _ws_call(q, k, v, kvl, out_dtype=torch.float32, workspace="auto"):
     (1, 2048, 16384, 2, 128, None, 8, 22),    # 16 items split 8 ways, 16 tiles per piece
     (1, 6400, 6400, 2, 128, 6390, 3, 23),     # 50 tiles in 3 uneven ranges (16, 17, 17)
     (1, 5000, 6000, 3, 64, 5999, 2, 24),      # D = 64, ragged query block (5000 = 19*256 + 136)
+    (2, 4500, 4500, 3, 128, 4400, 2, 25),     # B = 2: 108 items split in two, ragged query blocks
 ])
 def test_split_matches_oracle_whole(B, Nq, Nkv, H, D, kvl, f_152, seed):
     import dit_long_sequence_gb300 as dl
