@@ -119,11 +119,22 @@ cudaError_t merge_impl(const MergeArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const int sms = device_sm_count(dev);
-    int64_t blocks = (n_pos + kMergeWarps - 1) / kMergeWarps;
-    const int64_t cap = static_cast<int64_t>(sms) * 16;
-    if (blocks > cap) blocks = cap;
+    // Positions are dealt to warps round-robin.  Launch no more blocks than
+    // fit on the GPU at once (the 32 KB weight table per block bounds that),
+    // take the fewest rounds those warps allow, then only as many warps as the
+    // rounds need: every warp gets the same count (give or take one) and no
+    // late wave of blocks or half-empty last round stretches the tail.
+    auto kern = lse_merge_kernel<D, BF16>;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMergeThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t cap_warps = static_cast<int64_t>(sms) * per_sm * kMergeWarps;
+    const int64_t rounds = (n_pos + cap_warps - 1) / cap_warps;
+    const int64_t warps = (n_pos + rounds - 1) / rounds;
+    int64_t blocks = (warps + kMergeWarps - 1) / kMergeWarps;
     if (blocks < 1) blocks = 1;
-    lse_merge_kernel<D, BF16><<<static_cast<unsigned>(blocks), kMergeThreads, 0, stream>>>(a, n_pos);
+    kern<<<static_cast<unsigned>(blocks), kMergeThreads, 0, stream>>>(a, n_pos);
     return cudaGetLastError();
 }
 
