@@ -32,6 +32,19 @@ constexpr int kMergeThreads = 32 * kMergeWarps;
 constexpr int kMaxChunks = 64;
 constexpr int kGroup = 16;  // chunk loads in flight per lane and row
 
+// Blocks for need_blocks block-rounds of grid-stride work: no more than fit on
+// the GPU at once (per_sm resident blocks per SM), spread so that every block
+// runs the same number of rounds, give or take one.  The merge's per-position
+// work is coarse, so a grid of several waves (or a partly empty last round)
+// shows in its tail; the pure streaming kernels (layout, cast, norm + RoPE)
+// measured faster with oversubscribed grids.
+inline int64_t balanced_blocks(int64_t need_blocks, int per_sm, int sms) {
+    if (need_blocks < 1) return 1;
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+    const int64_t rounds = (need_blocks + cap - 1) / cap;
+    return (need_blocks + rounds - 1) / rounds;
+}
+
 template <int D, bool OUT_BF16>
 __global__ void __launch_bounds__(kMergeThreads, 4) lse_merge_kernel(const MergeArgs a, int64_t n_pos) {
     constexpr int LPR = D / 4;    // lanes per row
@@ -119,21 +132,13 @@ cudaError_t merge_impl(const MergeArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const int sms = device_sm_count(dev);
-    // Positions are dealt to warps round-robin.  Launch no more blocks than
-    // fit on the GPU at once (the 32 KB weight table per block bounds that),
-    // take the fewest rounds those warps allow, then only as many warps as the
-    // rounds need: every warp gets the same count (give or take one) and no
-    // late wave of blocks or half-empty last round stretches the tail.
+    // Positions are dealt to warps round-robin: resident blocks only, every
+    // warp the same count of positions (give or take one).
     auto kern = lse_merge_kernel<D, BF16>;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMergeThreads, 0);
     if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    const int64_t cap_warps = static_cast<int64_t>(sms) * per_sm * kMergeWarps;
-    const int64_t rounds = (n_pos + cap_warps - 1) / cap_warps;
-    const int64_t warps = (n_pos + rounds - 1) / rounds;
-    int64_t blocks = (warps + kMergeWarps - 1) / kMergeWarps;
-    if (blocks < 1) blocks = 1;
+    const int64_t blocks = balanced_blocks((n_pos + kMergeWarps - 1) / kMergeWarps, per_sm, sms);
     kern<<<static_cast<unsigned>(blocks), kMergeThreads, 0, stream>>>(a, n_pos);
     return cudaGetLastError();
 }
