@@ -117,22 +117,28 @@ dit_status_t dit_attn_fwd(const void *q, const void *k, const void *v,
  * item count is not a multiple of the SM count, the last partial wave leaves
  * most SMs idle for a whole item's time.  With a workspace, each item of that
  * partial wave is split into f contiguous key ranges (f = SMs / leftover items
- * clamped to [2, 8], at least 16 key tiles of 128 each), run by a second
- * kernel launched as a programmatic dependent launch so that its CTAs fill the
- * SMs as the last whole items drain, and their normalised partial (O, LSE)
- * pairs are combined by a third kernel with the
- * exact merge of "Scaling Video Generation Across NVL72 rack with
- * TensorRT-LLM", "Ring Attention", paragraph "Online-softmax merge" (the pages
- * have no counterpart for the scheduling itself; the combine is that merge).
- * Results equal dit_attn_fwd's up to fp32 rounding of the merge.
+ * clamped to [2, 8], at least 16 key tiles of 128 each).  A second kernel,
+ * launched as a programmatic dependent launch, runs the ranges so that its
+ * CTAs fill the SMs as the last whole items drain; a third combines each
+ * item's normalised partial (O, LSE) pairs with the exact merge of "Scaling
+ * Video Generation Across NVL72 rack with TensorRT-LLM", "Ring Attention",
+ * paragraph "Online-softmax merge" (the pages have no counterpart for the
+ * scheduling itself; the combine is that merge).
+ *
+ * Results: items that are not split are bit-identical to dit_attn_fwd's.
+ * Split items differ by the bf16 rounding of the probabilities P (each range
+ * rounds them against its own running maximum) -- a few 1e-4 at most at 8k
+ * keys, both within the same tolerance of the exact result -- and their LSE by
+ * fp32 rounding.  The call is deterministic (fixed merge order).
  *
  * workspace  NULL (then exactly dit_attn_fwd), or device memory of at least
  *        dit_attn_fwd_workspace_bytes(B, Nq, H, D, key_valid_len) bytes, 16-byte
  *        aligned, owned by the caller and not used by anything else until the
- *        stream has passed the call.  A smaller non-zero size is
- *        DIT_ERR_INVALID_ARG.
+ *        stream has passed the call.  A non-NULL workspace smaller than that
+ *        is DIT_ERR_INVALID_ARG (nothing is enqueued).
  * Other arguments and results as dit_attn_fwd.  Enqueues one kernel, or three
- * when a split applies.
+ * when a split applies; work queued behind the call on the same stream sees
+ * all of its outputs.
  */
 dit_status_t dit_attn_fwd_ws(const void *q, const void *k, const void *v,
                              const dit_attn_strides_t *strides,
@@ -143,12 +149,12 @@ dit_status_t dit_attn_fwd_ws(const void *q, const void *k, const void *v,
                              dit_stream_t stream);
 
 /*
- * dit_attn_fwd_workspace_bytes -- workspace bytes dit_attn_fwd_ws (and
- * dit_attn_fwd_fp8_ws, D = 128) uses for this
- * shape on the CURRENT device (the plan depends on its SM count): the split
- * pieces' fp32 partial O (256 x D per piece) and LSE (256 per piece).  0 when
- * no split helps (the item count is a multiple of the SM count, the keys are
- * too few, or there is nothing to compute); D outside {64, 128} gives 0.
+ * dit_attn_fwd_workspace_bytes -- workspace bytes that dit_attn_fwd_ws (and
+ * dit_attn_fwd_fp8_ws, D = 128) use for this shape on the CURRENT device (the
+ * plan depends on its SM count): the split pieces' fp32 partial O (256 x D per
+ * piece) and LSE (256 per piece).  0 when no split helps (the item count is a
+ * multiple of the SM count, the keys are too few, or there is nothing to
+ * compute); D outside {64, 128} gives 0.  Host only, one cached device query.
  */
 size_t dit_attn_fwd_workspace_bytes(int B, int Nq, int H, int D, int key_valid_len);
 
