@@ -48,11 +48,13 @@ struct AttnArgs {
     float* ws_lse;
 };
 
-// Tail split of the bf16 attention grid: the last partial wave's items
-// (tail = items % sms of them) are cut into f = sms / tail key ranges (one
-// wave of pieces when the grid has no whole wave), at least 2 and at most
-// kMaxSplit, each range at least kMinSplitTiles key tiles; no split when even
-// 2 ranges would be shorter.
+// Tail split of the attention grid: the last partial wave's items (tail =
+// items % sms of them) are cut into f = sms / tail key ranges -- one wave of
+// pieces -- at most kMaxSplit, each range at least kMinSplitTiles key tiles.
+// Behind whole waves f is at least 2 even when tail > sms / 2: the pieces
+// then even out the end of the grid.  A grid that is one partial wave and
+// fills more than half the SMs is not split (two waves of half items would
+// take as long as one of whole items).
 struct SplitPlan {
     int64_t first;   // items before the split ones
     int f;           // pieces per split item (1 = no split)
@@ -66,7 +68,7 @@ inline SplitPlan plan_tail_split(int64_t items, int n_kv_tiles, int sms) {
     const int64_t tail = items % sms;
     if (tail == 0) return p;
     int64_t f = sms / tail;
-    if (f < 2) f = 2;
+    if (items > sms && f < 2) f = 2;
     if (f > kMaxSplit) f = kMaxSplit;
     if (f > n_kv_tiles / kMinSplitTiles) f = n_kv_tiles / kMinSplitTiles;
     if (f < 2) return p;

@@ -116,8 +116,9 @@ dit_status_t dit_attn_fwd(const void *q, const void *k, const void *v,
  * The GPU runs one CTA per (b, h, 256-row query block) work item.  When the
  * item count is not a multiple of the SM count, the last partial wave leaves
  * most SMs idle for a whole item's time.  With a workspace, each item of that
- * partial wave is split into f contiguous key ranges (f = SMs / leftover items
- * clamped to [2, 8], at least 16 key tiles of 128 each).  A second kernel,
+ * partial wave is split into f contiguous key ranges (f = SMs / leftover items,
+ * at most 8, at least 2 behind whole waves; each range at least 16 key tiles of
+ * 128; no split for a single partial wave that fills more than half the SMs).  A second kernel,
  * launched as a programmatic dependent launch, runs the ranges so that its
  * CTAs fill the SMs as the last whole items drain; a third combines each
  * item's normalised partial (O, LSE) pairs with the exact merge of "Scaling
