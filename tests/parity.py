@@ -74,19 +74,36 @@ def compare(O_gpu: np.ndarray, L_gpu: np.ndarray, O_ref: np.ndarray, L_ref: np.n
 # ---------------------------------------------------------------- FP8 path
 # The FP8 kernel rounds each probability P to E4M3 before the P.V product
 # (relative rounding error |delta| <= 2^-4 for the normal range; P's row max
-# is >= 2^7 so subnormal P are >= 2^-16 below it).  Against the fp64 oracle
-# on the same E4M3 inputs:
-#   |O - O_ref| = |sum_j P_j delta_j v_j| / sum_j P_j <= 2^-4 * max_j |v_j|,
-# the hard per-element bound (plus 1e-3 for the fp32 arithmetic); and, delta
-# being zero-mean with RMS 2^-4 * sqrt(E[1/m^2] / 3) ~= 0.027 over mantissas
-# m in [1, 2), the per-head relative L2 error of O is ~0.027 -- gated at 0.04.
+# is >= 2^7 so subnormal P are >= 2^-16 below it).  LSE and the divisor l come
+# from the unrounded fp32 P, so against the fp64 oracle on the same E4M3 inputs
+#   e = O - O_ref = sum_j w_j delta_j v_j,   w_j = P_j / sum_k P_k.
+# Hard per-element bound: |e| <= 2^-4 * max_j |v_j| (plus 1e-3 for the fp32
+# arithmetic).
+# Statistical bounds: delta = u / m with u uniform in [-2^-4, 2^-4] (half the
+# E4M3 spacing at mantissa m in [1, 2)), so its RMS is
+#   sigma = 2^-4 * sqrt(E[1/m^2] / 3) <= 2^-4 / sqrt(3) ~= 0.036
+# (m >= 1), and ~0.027 for the near log-uniform mantissas of exponentials.
+# With delta zero-mean and independent of v,
+#   E[e^2] = sigma^2 * E[sum_j w_j^2 v_j^2],
+# and for v drawn independently of the keys' weights E[O_ref^2] has the same
+# value, so RMS(e) ~= sigma * RMS(O_ref).  Gates:
+#   * per-head relative L2 of O <= 0.04 (sigma ~0.027 with margin);
+#   * mean |e| <= 2^-4 / sqrt(3) * RMS(O_ref) + 1e-5: mean |e| <= RMS(e), and
+#     the worst-case sigma bounds RMS(e) (1e-5 covers the fp32 arithmetic).
 # LSE comes from the unrounded fp32 P: the bf16 gate (1e-3) applies.
 FP8_O_REL_L2 = 0.04
+FP8_DELTA_RMS_MAX = 2.0 ** -4 / np.sqrt(3.0)
+
+
+def fp8_o_mean_bound(O_ref: np.ndarray) -> float:
+    """The FP8 mean-abs gate on O for this reference (see the derivation above)."""
+    rms = float(np.sqrt(np.mean(np.square(O_ref)))) if O_ref.size else 0.0
+    return FP8_DELTA_RMS_MAX * rms + 1e-5
 
 
 def compare_fp8(O_gpu, L_gpu, O_ref, L_ref, v_absmax: float, head_axes=(0, 1)):
     return compare(O_gpu, L_gpu, O_ref, L_ref, head_axes=head_axes, o_max=2.0 ** -4 * v_absmax + 1e-3,
-                   o_mean=float("inf"), lse_max=LSE_MAX_ABS, rel_l2=FP8_O_REL_L2)
+                   o_mean=fp8_o_mean_bound(O_ref), lse_max=LSE_MAX_ABS, rel_l2=FP8_O_REL_L2)
 
 
 def host_u8(t: torch.Tensor) -> np.ndarray:
