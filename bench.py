@@ -3,15 +3,17 @@ fraction of the measured dense-bf16 peak.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
-A step is one pass of the hot path over one batch of synthetic input.  For the
-default workload (ltx2_padded: B=1, H=32, D=128, 24,200 valid tokens padded to
-24,576, key-only mask) the step is: split the fused [B, T, 3, H, D] QKV
-projection into head-major Q/K/V (dit_qkv_to_head_major), then attention with
-LSE over the head-major views (dit_attn_fwd_ws: dit_attn_fwd with a workspace
-that splits the grid's last partial wave over key ranges, plus the small
-kernel that merges those pieces).  Other workloads: cosmos3_nano
-(attention straight on strided views of the fused buffer), wan22_a14b
-(separate Q/K/V), ring9 (9 key chunks, 9 attention calls + dit_attn_lse_merge),
+A step is one pass of the hot path over one batch of synthetic input.  The
+default workload is ring9, the largest single-GPU configuration: B=1, H=64,
+D=128, 147,456 tokens, the keys split into 9 chunks of 16,384.  Its step is 9
+attention calls with LSE (dit_attn_fwd_ws: dit_attn_fwd with a workspace that
+splits the grid's last partial wave over key ranges, plus the small kernel that
+merges those pieces), each on one key chunk, writing its (O, LSE) partial
+straight into a per-row interleaved buffer, then one dit_attn_lse_merge of the
+9 partials.  Other workloads: ltx2_padded (split of the fused
+[B, T, 3, H, D] projection into head-major Q/K/V by dit_qkv_to_head_major,
+then attention with the key-only mask), cosmos3_nano (attention straight on
+strided views of the fused buffer), wan22_a14b (separate Q/K/V),
 ltx2_padded_fp8 / wan22_a14b_fp8 (one-pass E4M3 cast of the stacked buffer,
 then dit_attn_fwd_fp8_ws).
 
@@ -31,7 +33,6 @@ import hashlib
 import json
 import math
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -59,6 +60,8 @@ def load_peaks():
 
 
 def kernel_source_hash(main: str = "attn_fwd.cu") -> str:
+    """Hash of the files an attention kernel is compiled from (its .cu, the PTX
+    wrappers and the kernel-argument header); host-only files are left out."""
     h = hashlib.sha256()
     for fn in (main, "ptx.cuh", "internal.h"):
         with open(os.path.join(ROOT, "dit_long_sequence_gb300", "csrc", fn), "rb") as f:
@@ -67,18 +70,19 @@ def kernel_source_hash(main: str = "attn_fwd.cu") -> str:
 
 
 def profiled_traffic(workload: str):
-    """dram bytes per attention launch from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
-    fp8 = workload.endswith("_fp8")
-    p = os.path.join(ROOT, "profiles", f"{'attn_fwd_fp8_' + workload[:-4] if fp8 else 'attn_fwd_' + workload}.md")
-    if not os.path.exists(p):
+    """DRAM bytes per attention call for this workload from the ncu record
+    (profiles/dram_traffic.json), if it was taken on the current kernel
+    source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
         return None
-    text = open(p, encoding="utf-8").read()
-    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
-    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash("attn_fwd_fp8.cu" if fp8 else "attn_fwd.cu"):
-        return None
-    return float(m_bytes.group(1))
+    with open(path, encoding="utf-8") as f:
+        rec = json.load(f)
+    main = "attn_fwd_fp8.cu" if workload.endswith("_fp8") else "attn_fwd.cu"
+    for e in rec.get("entries", []):
+        if e.get("workload") == workload and e.get("kernel_source_sha256_16") == kernel_source_hash(main):
+            return float(e["dram_bytes_per_call"])
+    return None
 
 
 class ClockSampler:
@@ -560,7 +564,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=None,
                     help="timed steps (default: about 1.5 s of timed work)")
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="ltx2_padded")
+    ap.add_argument("--workload", default="ring9")
     ap.add_argument("--heads", type=int, default=None,
                     help="override the head count (small profiling cases of the same kernel)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])

@@ -14,6 +14,7 @@
 
 #include "dit_attn.h"
 #include "internal.h"
+#include "split_plan.h"
 
 namespace dit {
 
@@ -50,36 +51,74 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// The current context's unique id (cuCtxGetCurrent + cuCtxGetId through the
+// driver entry points), 0 if there is none.  A device's primary context is
+// replaced by cudaDeviceReset; module globals then live at new addresses, so
+// cached symbol addresses are keyed on this id and looked up again for a new
+// context.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    if (get_current == nullptr || get_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id + 1;   // never 0 for a live context
+}
+
+// Per-device cache of a module global's device address, valid for one context.
+struct SymbolCache {
+    std::mutex mu;
+    unsigned long long ctx_id = 0;
+    void* addr = nullptr;
+};
+
 struct DeviceCache {
-    std::atomic<unsigned int*> status{nullptr};
+    SymbolCache status;
+    SymbolCache noalloc_occ;
     std::atomic<int> sm_count{0};
-    std::atomic<uint32_t*> noalloc_occ{nullptr};
 };
 DeviceCache g_dev[kMaxDevices];
 
-unsigned int* status_word(int dev) {
-    if (dev < 0 || dev >= kMaxDevices) return nullptr;
-    unsigned int* p = g_dev[dev].status.load(std::memory_order_acquire);
-    if (p == nullptr) {
-        void* addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return nullptr;
-        p = static_cast<unsigned int*>(addr);
-        g_dev[dev].status.store(p, std::memory_order_release);
-    }
-    return p;
+// Device address of `symbol` in the current context of the current device:
+// looked up with cudaGetSymbolAddress once per context (the first lookup also
+// makes the runtime set up the device's primary context if it has not yet).
+template <typename T>
+T* symbol_address(SymbolCache& c, const void* symbol) {
+    unsigned long long id = current_context_id();
+    std::lock_guard<std::mutex> lock(c.mu);
+    if (id != 0 && c.addr != nullptr && c.ctx_id == id) return static_cast<T*>(c.addr);
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, symbol) != cudaSuccess) return nullptr;
+    c.addr = addr;
+    c.ctx_id = current_context_id();   // 0 (never matches) if it cannot be read
+    return static_cast<T*>(addr);
 }
 
-// Device address of the no-alloc occupancy scratch, looked up once per device.
+unsigned int* status_word(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    return symbol_address<unsigned int>(g_dev[dev].status, g_status_word);
+}
+
+// Device address of the no-alloc occupancy scratch in the current context.
 uint32_t* noalloc_scratch(int dev) {
     if (dev < 0 || dev >= kMaxDevices) return nullptr;
-    uint32_t* p = g_dev[dev].noalloc_occ.load(std::memory_order_acquire);
-    if (p == nullptr) {
-        void* addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_noalloc_occ) != cudaSuccess) return nullptr;
-        p = static_cast<uint32_t*>(addr);
-        g_dev[dev].noalloc_occ.store(p, std::memory_order_release);
-    }
-    return p;
+    return symbol_address<uint32_t>(g_dev[dev].noalloc_occ, g_noalloc_occ);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -131,10 +170,6 @@ int device_sm_count(int dev) {
 }  // namespace dit
 
 using namespace dit;
-
-extern "C" {
-
-}  // extern "C"
 
 namespace {
 

@@ -2,14 +2,18 @@
  * dit_attn.h -- C ABI of libditattn.so: dense bidirectional long-sequence
  * attention for DiT video denoising on one NVIDIA GB300 (sm_103a).
  *
- * Three operations, all asynchronous on a caller-supplied CUDA stream:
+ * Entry points, all asynchronous on a caller-supplied CUDA stream:
  *
  *   dit_attn_fwd           softmax(scale * Q K^T) V plus the per-row
  *                          log-sum-exp, Q/K/V read through arbitrary
  *                          (b, n, h) strides, key-only padding mask.
  *   dit_attn_fwd_ws        the same with a workspace that balances the
  *                          grid's last partial wave.
- *   dit_attn_fwd_masked    the same with a general (B, Nq, Nkv) bit mask.
+ *   dit_attn_fwd_masked    the same with a general (B, Nq, Nkv) bit mask
+ *                          (dit_attn_fwd_masked_noalloc: its scratch inside
+ *                          the library instead of a caller workspace).
+ *   dit_attn_fwd_accumulate  one more key chunk folded into a running
+ *                          (O, LSE) pair.
  *   dit_attn_lse_merge     exact combine of (O, LSE) partials computed over
  *                          disjoint key chunks.
  *   dit_qkv_to_head_major  split of a fused [B, N, 3, H, D] projection
@@ -25,7 +29,8 @@
  * ---------------------------------------
  * - All tensor pointers are DEVICE pointers owned by the caller.  The library
  *   allocates no memory, copies nothing between host and device and keeps no
- *   per-call state; per-device caches hold only kernel attributes.
+ *   per-call state; per-device caches hold kernel attributes, the SM count
+ *   and the device addresses of the library's own globals.
  * - Strides are in ELEMENTS, not bytes.
  * - Argument, shape, stride and alignment checks run on the host before any
  *   launch.  A failed check returns a non-zero status and enqueues nothing.
@@ -156,6 +161,9 @@ dit_status_t dit_attn_fwd_ws(const void *q, const void *k, const void *v,
  * piece) and LSE (256 per piece).  0 when no split helps (the item count is a
  * multiple of the SM count, the keys are too few, or there is nothing to
  * compute); D outside {64, 128} gives 0.  Host only, one cached device query.
+ * The size holds for the device current at query time (and any device with
+ * the same SM count): a call on a device with more SMs can plan a larger
+ * split and then refuses a workspace sized elsewhere (DIT_ERR_INVALID_ARG).
  */
 size_t dit_attn_fwd_workspace_bytes(int B, int Nq, int H, int D, int key_valid_len);
 
@@ -215,7 +223,10 @@ dit_status_t dit_attn_fwd_masked(const void *q, const void *k, const void *v,
  *     key_valid_len) exceeds 262,144 bytes (checked before anything is enqueued);
  *   - calls on one device must be ordered (the same stream, or streams joined
  *     by events): two in flight at once would share the array.
- * Allocates nothing; the array's address is looked up once per device.
+ * Allocates nothing.  The array's device address is looked up with
+ * cudaGetSymbolAddress on the first call in each CUDA context of a device
+ * and cached for that context; after cudaDeviceReset (a new primary context,
+ * where the array has a new address) the next call looks it up again.
  */
 dit_status_t dit_attn_fwd_masked_noalloc(const void *q, const void *k, const void *v,
                                          const dit_attn_strides_t *strides,

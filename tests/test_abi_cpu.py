@@ -1,14 +1,34 @@
 """Host-side checks of the C ABI that need no GPU.
 
 The library loads and exports every entry point include/dit_attn.h declares,
-and every argument check returns its status before anything touches a device
-(the pointers passed here are never dereferenced).
+and every argument check returns its status before anything touches a device.
+The argument checks pass made-up device addresses, so they run only in a
+process that sees no CUDA device: there a check that ever stopped returning
+first could not launch anything.  Where a device is visible (an unfiltered
+pytest on a GPU machine), one test re-runs them in a child process with
+CUDA_VISIBLE_DEVICES="".
 """
 import ctypes
 import os
 import re
+import subprocess
+import sys
 
 import pytest
+
+
+def _device_visible() -> bool:
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:  # pragma: no cover
+        return False
+
+
+DEVICE_VISIBLE = _device_visible()
+# made-up device addresses: only where no device can be reached
+deviceless = pytest.mark.skipif(DEVICE_VISIBLE, reason="passes made-up device addresses; re-run in a "
+                                                      "deviceless child by test_argument_checks_in_a_deviceless_child")
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -55,6 +75,7 @@ def _fwd(lib, **kw):
                                   args["dt"], args["lse"], None)
 
 
+@deviceless
 def test_attn_fwd_argument_checks(lib):
     E = lib
     assert _fwd(lib, D=96) == E.DIT_ERR_UNSUPPORTED
@@ -81,6 +102,7 @@ def test_attn_fwd_argument_checks(lib):
     assert _fwd(lib, Nq=0) == E.DIT_OK
 
 
+@deviceless
 def test_merge_argument_checks(lib):
     f = lib.raw().dit_attn_lse_merge
     ok_args = (FAKE, 1 * 8 * 4 * 128, 128, FAKE, 1 * 4 * 8, 2, 1, 8, 4, 128, FAKE, lib.DIT_F32, FAKE, None)
@@ -103,6 +125,7 @@ def test_merge_argument_checks(lib):
     assert call(B=0) == lib.DIT_OK
 
 
+@deviceless
 def test_layout_argument_checks(lib):
     f = lib.raw().dit_qkv_to_head_major
     assert f(FAKE, 0, 3 * 4 * 12, 1, 8, 4, 12, FAKE, FAKE, FAKE, None) == lib.DIT_ERR_UNSUPPORTED  # D % 8
@@ -133,6 +156,7 @@ def _fwd8(lib, **kw):
                                       args["dq"], args["dk"], args["dv"], args["out"], args["dt"], args["lse"], None)
 
 
+@deviceless
 def test_attn_fwd_fp8_argument_checks(lib):
     E = lib
     assert _fwd8(lib, D=64) == E.DIT_ERR_UNSUPPORTED            # head dim 128 only
@@ -150,6 +174,7 @@ def test_attn_fwd_fp8_argument_checks(lib):
     assert _fwd8(lib, B=0, q=None, out=None, lse=None) == E.DIT_OK
 
 
+@deviceless
 def test_cast_fp8_argument_checks(lib):
     f = lib.raw().dit_qkv_cast_fp8
     ok = (FAKE, 0, 3 * 4 * 64, 1, 8, 4, 64, 1.0, 2.0, 3.0, FAKE, None)
@@ -172,6 +197,7 @@ def test_cast_fp8_argument_checks(lib):
     assert call(N=0) == lib.DIT_OK
 
 
+@deviceless
 def test_norm_rope_argument_checks(lib):
     f = lib.raw().dit_qkv_norm_rope_to_head_major
     ok = [FAKE, 0, 3 * 4 * 64, 1, 8, 4, 64, FAKE, FAKE, 1e-6, FAKE, FAKE + 4096, FAKE, FAKE, FAKE, None]
@@ -193,6 +219,7 @@ def test_norm_rope_argument_checks(lib):
     assert call(N=0) == lib.DIT_OK
 
 
+@deviceless
 def test_masked_argument_checks(lib):
     st = lib.AttnStrides(*(lib.Strides4(8 * 128 * 4, 4 * 128, 128, 1) for _ in range(4)))
     f = lib.raw().dit_attn_fwd_masked
@@ -216,6 +243,7 @@ def test_masked_argument_checks(lib):
     assert ws(2, 256, 128) == 8 and ws(0, 10, 10) == 0 and ws(1, 10, 0) == 0
 
 
+@deviceless
 def test_attn_fwd_ws_argument_checks(lib):
     st = lib.AttnStrides(*(lib.Strides4(8 * 128 * 4, 4 * 128, 128, 1) for _ in range(4)))
     f = lib.raw().dit_attn_fwd_ws
@@ -237,3 +265,26 @@ def test_attn_fwd_ws_argument_checks(lib):
     wsb = lib.raw().dit_attn_fwd_workspace_bytes
     assert wsb(1, 24576, 32, 96, 24200) == 0          # unsupported D
     assert wsb(0, 24576, 32, 128, 24200) == 0 and wsb(1, 24576, 32, 128, 0) == 0
+
+
+@deviceless
+def test_noalloc_rejects_maps_beyond_its_array_before_launching(lib):
+    st = lib.AttnStrides(*(lib.Strides4(8 * 128 * 4, 4 * 128, 128, 1) for _ in range(4)))
+    # B=64, 65,536 rows, 65,536 keys: 64 * 256 blocks * 16 words * 4 B = 1 MiB > 256 KiB
+    rc = lib.raw().dit_attn_fwd_masked_noalloc(FAKE, FAKE, FAKE, ctypes.byref(st), 64, 65536, 65536, 4, 128, 65536,
+                                               FAKE, 0, 2048, 65536, 0.088, FAKE, lib.DIT_F32, FAKE, None)
+    assert rc == lib.DIT_ERR_UNSUPPORTED
+
+
+def test_argument_checks_in_a_deviceless_child():
+    """Where this process sees a CUDA device, the made-up-address checks run in
+    a child process that sees none."""
+    if not DEVICE_VISIBLE:
+        pytest.skip("no device visible: the checks above ran in this process")
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider", "-m", "not gpu",
+                        os.path.abspath(__file__)], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+    m = re.search(r"(\d+) passed", r.stdout)
+    n_checks = sum(1 for line in open(os.path.abspath(__file__)) if line.startswith("@deviceless"))
+    assert m and int(m.group(1)) >= n_checks, r.stdout[-2000:]

@@ -106,9 +106,12 @@ def test_traffic_only_reported_for_the_profiled_kernel_source(tmp_path, monkeypa
     for fn in ("attn_fwd.cu", "ptx.cuh", "internal.h"):
         (tmp_path / "dit_long_sequence_gb300" / "csrc" / fn).write_text(fn)
     h = bench.kernel_source_hash()
-    (prof / "attn_fwd_w.md").write_text(f"kernel_source_sha256_16: {h}\ndram_bytes_per_launch: 1.5e9\n")
+    rec = {"entries": [{"workload": "w", "kernel_source_sha256_16": h, "dram_bytes_per_call": 1.5e9}]}
+    (prof / "dram_traffic.json").write_text(json.dumps(rec))
     assert bench.profiled_traffic("w") == 1.5e9
-    (prof / "attn_fwd_w.md").write_text("kernel_source_sha256_16: 0000000000000000\ndram_bytes_per_launch: 1.5e9\n")
+    assert bench.profiled_traffic("other") is None
+    rec["entries"][0]["kernel_source_sha256_16"] = "0000000000000000"
+    (prof / "dram_traffic.json").write_text(json.dumps(rec))
     assert bench.profiled_traffic("w") is None
 
 

@@ -1,5 +1,5 @@
 """Host-side checks of the tail-split plan (plan_tail_split and
-split_workspace_bytes in csrc/internal.h), compiled into a small host
+split_workspace_bytes in csrc/split_plan.h), compiled into a small host
 program with g++ -- no GPU needed.
 
 The plan cuts the last partial wave of work items (items mod SMs of them)
@@ -21,7 +21,7 @@ CSRC = os.path.join(ROOT, "dit_long_sequence_gb300", "csrc")
 
 HARNESS = r"""
 #include <cstdio>
-#include "internal.h"
+#include "split_plan.h"
 int main() {
     long long items; int tiles, sms, D;
     while (std::scanf("%lld %d %d %d", &items, &tiles, &sms, &D) == 4) {
