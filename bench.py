@@ -570,6 +570,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-kernel-legs", action="store_true",
+                    help="skip the secondary HBM-kernel timing legs (small device footprint for profiling runs)")
     ap.add_argument("--masked", action="store_true",
                     help="also time the general-mask attention variant on this workload (bf16 workloads)")
     args = ap.parse_args(argv)
@@ -644,16 +646,16 @@ def main(argv=None):
 
     # ---------------- secondary HBM-bound kernels
     extra = {}
-    lay = time_layout_kernel(step)
+    lay = None if args.no_kernel_legs else time_layout_kernel(step)
     if lay is not None:
         gbs = lay[0] / (lay[1] * 1e-3) / 1e9
         extra["cast_fp8" if w.fp8 else "layout"] = {"bytes": lay[0], "ms": lay[1], "GB/s": gbs, "frac_hbm": gbs / float(peaks["hbm_gbs"])}
-    nr = time_norm_rope_kernel(step)
+    nr = None if args.no_kernel_legs else time_norm_rope_kernel(step)
     if nr is not None:
         gbs = nr[0] / (nr[1] * 1e-3) / 1e9
         extra["layout_norm_rope"] = {"bytes": nr[0], "ms": nr[1], "GB/s": gbs,
                                      "frac_hbm": gbs / float(peaks["hbm_gbs"])}
-    for il, key in ((True, "merge_n9_interleaved"), (False, "merge_n9_chunk_major")):
+    for il, key in (() if args.no_kernel_legs else ((True, "merge_n9_interleaved"), (False, "merge_n9_chunk_major"))):
         mb, mms = time_merge_kernel(dev, w.B, w.N, w.H, w.D, n_chunks=9, interleaved=il)
         mgbs = mb / (mms * 1e-3) / 1e9
         extra[key] = {"bytes": mb, "ms": mms, "GB/s": mgbs, "frac_hbm": mgbs / float(peaks["hbm_gbs"])}

@@ -5,6 +5,11 @@ element strides and the current CUDA stream; every step of the computation
 runs in the library's kernels.  PyTorch supplies device memory and streams.
 There is no fallback: if the library is missing or a call fails, an exception
 is raised.
+
+With the environment variable DIT_ATTN_DEBUG=1 at import, the binding loads
+the debug library instead (libditattn_debug.so: the same kernels with
+in-kernel bounds checks, include/dit_attn_debug.h); load_debug_library()
+gives a handle to it beside the product library.
 """
 from __future__ import annotations
 
@@ -13,19 +18,22 @@ import os
 
 import torch
 
-from .build import LIB as _LIB_PATH
+from .build import DEBUG_LIB as _DEBUG_LIB_PATH
+from .build import LIB as _PRODUCT_LIB_PATH
 
+is_debug_library = os.environ.get("DIT_ATTN_DEBUG", "") == "1"
+_LIB_PATH = _DEBUG_LIB_PATH if is_debug_library else _PRODUCT_LIB_PATH
 library_path = _LIB_PATH
 
 if not os.path.exists(_LIB_PATH):
     raise ImportError(
-        f"libditattn.so not found at {_LIB_PATH}; build it first with "
+        f"{os.path.basename(_LIB_PATH)} not found at {_LIB_PATH}; build it first with "
         "`python -m dit_long_sequence_gb300.build` (or __graft_entry__.build())")
 
-_lib = ctypes.CDLL(_LIB_PATH)
-
-DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_ALIGNMENT, DIT_ERR_CUDA, DIT_ERR_TIMEOUT = range(6)
+DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_ALIGNMENT, DIT_ERR_CUDA, DIT_ERR_TIMEOUT, DIT_ERR_BOUNDS = \
+    range(7)
 DIT_BF16, DIT_F32 = 0, 1
+DIT_FAULT_NONE, DIT_FAULT_SKIP_LOAD, DIT_FAULT_SKIP_S_COMMIT, DIT_FAULT_SKIP_P_ARRIVE = range(4)
 
 
 class Strides4(ctypes.Structure):
@@ -38,47 +46,69 @@ class AttnStrides(ctypes.Structure):
 
 _vp, _i, _i64, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
 
-_lib.dit_attn_fwd.restype = _i
-_lib.dit_attn_fwd.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
-                              _vp, _i, _vp, _vp]
-_lib.dit_attn_fwd_ws.restype = _i
-_lib.dit_attn_fwd_ws.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
-                                 _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]
-_lib.dit_attn_fwd_workspace_bytes.restype = ctypes.c_size_t
-_lib.dit_attn_fwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
-_lib.dit_attn_fwd_accumulate.restype = _i
-_lib.dit_attn_fwd_accumulate.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
-                                         _vp, _vp, _vp]
-_lib.dit_attn_fwd_masked.restype = _i
-_lib.dit_attn_fwd_masked.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _vp, _i64,
-                                     _i64, _i, _f, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]
-_lib.dit_attn_fwd_masked_noalloc.restype = _i
-_lib.dit_attn_fwd_masked_noalloc.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _vp,
-                                             _i64, _i64, _i, _f, _vp, _i, _vp, _vp]
-_lib.dit_attn_masked_workspace_bytes.restype = ctypes.c_size_t
-_lib.dit_attn_masked_workspace_bytes.argtypes = [_i, _i, _i]
-_lib.dit_attn_fwd_fp8.restype = _i
-_lib.dit_attn_fwd_fp8.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f, _f, _f, _f,
+
+def _declare(lib):
+    """Argument and result types of the C ABI on a loaded library handle."""
+    lib.dit_attn_fwd.restype = _i
+    lib.dit_attn_fwd.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
                                   _vp, _i, _vp, _vp]
-_lib.dit_attn_fwd_fp8_ws.restype = _i
-_lib.dit_attn_fwd_fp8_ws.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f, _f, _f,
-                                     _f, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]
-_lib.dit_qkv_cast_fp8.restype = _i
-_lib.dit_qkv_cast_fp8.argtypes = [_vp, _i64, _i64, _i, _i, _i, _i, _f, _f, _f, _vp, _vp]
-_lib.dit_qkv_norm_rope_to_head_major.restype = _i
-_lib.dit_qkv_norm_rope_to_head_major.argtypes = [_vp, _i64, _i64, _i, _i, _i, _i, _vp, _vp, _f, _vp, _vp, _vp, _vp,
-                                                 _vp, _vp]
-_lib.dit_watchdog_selftest.restype = _i
-_lib.dit_watchdog_selftest.argtypes = [ctypes.c_uint32, _vp]
-_lib.dit_attn_lse_merge.restype = _i
-_lib.dit_attn_lse_merge.argtypes = [_vp, _i64, _i64, _vp, _i64, _i, _i, _i, _i, _i, _vp, _i, _vp, _vp]
-_lib.dit_qkv_to_head_major.restype = _i
-_lib.dit_qkv_to_head_major.argtypes = [_vp, _i64, _i64, _i, _i, _i, _i, _vp, _vp, _vp, _vp]
-_lib.dit_status_string.restype = ctypes.c_char_p
-_lib.dit_status_string.argtypes = [_i]
-_lib.dit_check_watchdog.restype = _i
-_lib.dit_check_watchdog.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
-_lib.dit_version.restype = ctypes.c_uint32
+    lib.dit_attn_fwd_ws.restype = _i
+    lib.dit_attn_fwd_ws.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
+                                     _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.dit_attn_fwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.dit_attn_fwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+    lib.dit_attn_fwd_accumulate.restype = _i
+    lib.dit_attn_fwd_accumulate.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f,
+                                             _vp, _vp, _vp]
+    lib.dit_attn_fwd_masked.restype = _i
+    lib.dit_attn_fwd_masked.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _vp, _i64,
+                                         _i64, _i, _f, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.dit_attn_fwd_masked_noalloc.restype = _i
+    lib.dit_attn_fwd_masked_noalloc.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _vp,
+                                                 _i64, _i64, _i, _f, _vp, _i, _vp, _vp]
+    lib.dit_attn_masked_workspace_bytes.restype = ctypes.c_size_t
+    lib.dit_attn_masked_workspace_bytes.argtypes = [_i, _i, _i]
+    lib.dit_attn_fwd_fp8.restype = _i
+    lib.dit_attn_fwd_fp8.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f, _f, _f, _f,
+                                      _vp, _i, _vp, _vp]
+    lib.dit_attn_fwd_fp8_ws.restype = _i
+    lib.dit_attn_fwd_fp8_ws.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f, _f, _f,
+                                         _f, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.dit_qkv_cast_fp8.restype = _i
+    lib.dit_qkv_cast_fp8.argtypes = [_vp, _i64, _i64, _i, _i, _i, _i, _f, _f, _f, _vp, _vp]
+    lib.dit_qkv_norm_rope_to_head_major.restype = _i
+    lib.dit_qkv_norm_rope_to_head_major.argtypes = [_vp, _i64, _i64, _i, _i, _i, _i, _vp, _vp, _f, _vp, _vp, _vp, _vp,
+                                                     _vp, _vp]
+    lib.dit_watchdog_selftest.restype = _i
+    lib.dit_watchdog_selftest.argtypes = [ctypes.c_uint32, _vp]
+    lib.dit_attn_lse_merge.restype = _i
+    lib.dit_attn_lse_merge.argtypes = [_vp, _i64, _i64, _vp, _i64, _i, _i, _i, _i, _i, _vp, _i, _vp, _vp]
+    lib.dit_qkv_to_head_major.restype = _i
+    lib.dit_qkv_to_head_major.argtypes = [_vp, _i64, _i64, _i, _i, _i, _i, _vp, _vp, _vp, _vp]
+    lib.dit_status_string.restype = ctypes.c_char_p
+    lib.dit_status_string.argtypes = [_i]
+    lib.dit_check_watchdog.restype = _i
+    lib.dit_check_watchdog.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.dit_version.restype = ctypes.c_uint32
+    if hasattr(lib, "dit_debug_configure"):
+        lib.dit_debug_configure.restype = _i
+        lib.dit_debug_configure.argtypes = [ctypes.c_uint32, _i, _i, ctypes.c_uint32, _i64]
+        lib.dit_debug_build.restype = ctypes.c_uint32
+    return lib
+
+
+_lib = _declare(ctypes.CDLL(_LIB_PATH))
+
+
+def load_debug_library():
+    """ctypes handle of libditattn_debug.so with the C ABI declared: every
+    dit_attn.h entry point plus dit_debug_configure / dit_debug_build.  Its
+    kernels and device status word are its own (check it with its own
+    dit_check_watchdog)."""
+    if not os.path.exists(_DEBUG_LIB_PATH):
+        raise ImportError(f"libditattn_debug.so not found at {_DEBUG_LIB_PATH}; build it first")
+    return _declare(ctypes.CDLL(_DEBUG_LIB_PATH))
+
 
 EXPORTS = ("dit_attn_fwd", "dit_attn_fwd_ws", "dit_attn_fwd_workspace_bytes", "dit_attn_fwd_masked", "dit_attn_fwd_masked_noalloc", "dit_attn_masked_workspace_bytes",
            "dit_attn_fwd_accumulate", "dit_attn_lse_merge", "dit_qkv_to_head_major",

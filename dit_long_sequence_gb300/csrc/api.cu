@@ -13,6 +13,9 @@
 #include <mutex>
 
 #include "dit_attn.h"
+#ifdef DIT_DEBUG
+#include "dit_attn_debug.h"
+#endif
 #include "internal.h"
 #include "split_plan.h"
 
@@ -32,6 +35,16 @@ namespace {
 
 constexpr unsigned long long kWatchdogNs = 2000000000ull;  // 2 s per bounded wait
 constexpr int kMaxDevices = 64;
+
+#ifdef DIT_DEBUG
+// Debug library: the fault, wait limit and O-extent shrink the next calls use
+// (dit_debug_configure).
+std::atomic<uint32_t> g_dbg_fault{0};
+std::atomic<int> g_dbg_block{0};
+std::atomic<int> g_dbg_index{0};
+std::atomic<unsigned long long> g_dbg_limit_ns{0};
+std::atomic<int64_t> g_dbg_out_shrink{0};
+#endif
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -303,6 +316,23 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
     a.ws_lse = split.n_ctas > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                                           split.n_ctas * 256 * D * 4)
                                 : nullptr;
+    a.B = B;
+    // extents of the debug library's bounds checks (unused by the product kernels)
+    a.dbg_fault = FAULT_NONE;
+    a.dbg_fault_cta = 0;
+    a.dbg_fault_index = 0;
+    a.dbg_o_elems = static_cast<int64_t>(B - 1) * so.b + static_cast<int64_t>(Nq - 1) * so.n +
+                    static_cast<int64_t>(H - 1) * so.h + D;
+    a.dbg_mask_words = a.mask == nullptr ? 0
+                                         : static_cast<int64_t>(B - 1) * a.mask_sb +
+                                               static_cast<int64_t>(a.mask_rows - 1) * a.mask_si + 4 * a.n_kv_tiles;
+#ifdef DIT_DEBUG
+    a.dbg_fault = g_dbg_fault.load();
+    a.dbg_fault_cta = g_dbg_block.load();
+    a.dbg_fault_index = g_dbg_index.load();
+    if (g_dbg_limit_ns.load() != 0) a.timeout_ns = g_dbg_limit_ns.load();
+    a.dbg_o_elems -= g_dbg_out_shrink.load();
+#endif
     const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = fp8 ? launch_attn_fwd_fp8(tq, tk, tv, a, B, out_dtype == DIT_BF16, cs)
                         : launch_attn_fwd(tq, tk, tv, a, B, D, out_dtype == DIT_BF16, accumulate, cs);
@@ -545,6 +575,7 @@ const char* dit_status_string(dit_status_t s) {
         case DIT_ERR_ALIGNMENT: return "DIT_ERR_ALIGNMENT: pointer or stride breaks the 16-byte rules";
         case DIT_ERR_CUDA: return "DIT_ERR_CUDA: a CUDA call failed";
         case DIT_ERR_TIMEOUT: return "DIT_ERR_TIMEOUT: a bounded in-kernel wait ran out";
+        case DIT_ERR_BOUNDS: return "DIT_ERR_BOUNDS: an in-kernel bounds check failed (debug library)";
     }
     return "unknown dit_status_t";
 }
@@ -569,9 +600,27 @@ dit_status_t dit_check_watchdog(dit_stream_t stream, uint32_t info[4]) {
     }
     if (info != nullptr)
         for (int i = 0; i < 4; ++i) info[i] = host[i];
-    return host[0] == 0 ? DIT_OK : DIT_ERR_TIMEOUT;
+    if (host[0] == 0) return DIT_OK;
+    return host[0] == static_cast<unsigned int>(DIT_ERR_BOUNDS) ? DIT_ERR_BOUNDS : DIT_ERR_TIMEOUT;
 }
 
-uint32_t dit_version(void) { return (0u << 16) | 1u; }
+uint32_t dit_version(void) { return (0u << 16) | 2u; }
+
+#ifdef DIT_DEBUG
+dit_status_t dit_debug_configure(uint32_t fault, int fault_block, int fault_index, uint32_t wait_limit_us,
+                                 int64_t out_extent_shrink) {
+    if (fault > FAULT_SKIP_P_ARRIVE || fault_block < 0 || fault_index < 0 || out_extent_shrink < 0)
+        return DIT_ERR_INVALID_ARG;
+    if (wait_limit_us != 0 && (wait_limit_us < 1000 || wait_limit_us > 2000000)) return DIT_ERR_INVALID_ARG;
+    g_dbg_fault.store(fault);
+    g_dbg_block.store(fault_block);
+    g_dbg_index.store(fault_index);
+    g_dbg_limit_ns.store(1000ull * wait_limit_us);
+    g_dbg_out_shrink.store(out_extent_shrink);
+    return DIT_OK;
+}
+
+uint32_t dit_debug_build(void) { return 1u; }
+#endif
 
 }  // extern "C"

@@ -74,6 +74,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "debug.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -136,6 +137,7 @@ struct Cfg {
     static constexpr int kBarOffset = (2 + kStages) * kTileBytes;
     static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kBarOffset + kNumBars * 8 + 16;
     static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(256 + 2 * D <= 512, "S0, S1, O0, O1 fit the 512 TMEM columns");
 };
 
 // ACCUM: fold this pass into an existing fp32 (O, LSE) pair instead of
@@ -192,6 +194,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = wk.h;
     const int b = wk.b;
     const int q_row0 = wk.q_row0;
+    // (debug library) the item and its key range lie inside the problem
+    if (!in_bounds(h >= 0 && h < a.H && b >= 0 && b < a.B && q_row0 >= 0 && q_row0 < a.Nq && k_begin >= 0 &&
+                       k_begin <= k_end && k_end <= a.n_kv_tiles,
+                   a.status, 0, BND_ITEM))
+        return;
     if constexpr (!PIECE && !ACCUM && !MASK) {
         // The piece kernel (if any) may start once every CTA here has begun;
         // the items it covers are the last in grid order and left to it.
@@ -252,25 +259,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int total = 2 * n_tiles;
             int issued = 0;
+            int withheld = -1;   // (debug library) the load skipped on request
             TileCursor cur(occ, k_begin, k_end);
             int key0 = 0;
             for (int i = 0; i < total; ++i) {
                 if ((i & 1) == 0) key0 = cur.next() * kBN;
+                if (!in_bounds(key0 >= 0 && key0 < a.kv_len, a.status, ROLE_LOAD, BND_KEY)) break;
                 const int slot = i % S;
                 const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
                 if (!wait_bounded(bar(C::kKVEmpty + slot), ph ^ 1u, wd, ROLE_LOAD, SITE_KV_EMPTY)) break;
+                issued = i + 1;
+                if (inject(a, FAULT_SKIP_LOAD, i)) {
+                    withheld = i;   // neither the arrive nor the copy: the slot never fills
+                    continue;
+                }
                 mbar_arrive_expect_tx(bar(C::kKVFull + slot), TILE);
                 const CUtensorMap* tm = (i & 1) ? &tm_v : &tm_k;
                 const uint32_t dst = sRing + slot * TILE;
                 for (int c = 0; c < D / 64; ++c)
                     tma_load_4d(dst + c * C::kBlockBytes, tm, bar(C::kKVFull + slot), c * 64, key0, h, b);
-                issued = i + 1;
             }
             if (issued < total || *abort_flag) {
                 // Winding down: wait (bounded) until every copy issued has landed.
                 for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
-                    wait_bounded(bar(C::kKVFull + i % S), static_cast<uint32_t>(i / S) & 1u, wd_drain,
-                                 ROLE_LOAD, SITE_LOAD_DRAIN);
+                    if (i != withheld)
+                        wait_bounded(bar(C::kKVFull + i % S), static_cast<uint32_t>(i / S) & 1u, wd_drain,
+                                     ROLE_LOAD, SITE_LOAD_DRAIN);
                 wait_bounded(bar(C::kQFull + 0), 0, wd_drain, ROLE_LOAD, SITE_LOAD_DRAIN);
                 wait_bounded(bar(C::kQFull + 1), 0, wd_drain, ROLE_LOAD, SITE_LOAD_DRAIN);
             }
@@ -305,10 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = wait_bounded(bar(C::kQFull + 0), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
                       wait_bounded(bar(C::kQFull + 1), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
                       wait_bounded(bar(C::kKVFull + 0), 0, wd, ROLE_MMA, SITE_KV_FULL);
+            // S_0 number n is ready (the debug library can withhold one signal)
+            auto commit_s0 = [&](int n) {
+                if (!inject(a, FAULT_SKIP_S_COMMIT, n)) umma_commit(bar(C::kSFull + 0));
+            };
             if (ok) {
                 tc_fence_after();
                 issue_qk(tS0, sQ, sRing);
-                umma_commit(bar(C::kSFull + 0));
+                commit_s0(0);
                 issue_qk(tS1, sQ + TILE, sRing);
                 umma_commit(bar(C::kSFull + 1));
                 umma_commit(bar(C::kKVEmpty + 0));
@@ -319,6 +337,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t k_addr = sRing + (ik % S) * TILE;
                 const bool more = j + 1 < n_tiles;
                 const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+                if (!in_bounds(v_addr >= sRing && v_addr + TILE <= sRing + S * TILE && k_addr >= sRing &&
+                                   k_addr + TILE <= sRing + S * TILE,
+                               a.status, ROLE_MMA, BND_SMEM))
+                    break;
                 ok = wait_bounded(bar(C::kKVFull + iv % S), static_cast<uint32_t>(iv / S) & 1u, wd, ROLE_MMA,
                                   SITE_KV_FULL) &&
                      wait_bounded(bar(C::kPFull + 0), ph, wd, ROLE_MMA, SITE_P_FULL);
@@ -331,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     tc_fence_after();
                     issue_qk(tS0, sQ, k_addr);
-                    umma_commit(bar(C::kSFull + 0));
+                    commit_s0(j + 1);
                 } else {
                     umma_commit(bar(C::kOFinal + 0));
                 }
@@ -373,7 +395,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         TileCursor cur(occ, k_begin, k_end);
         int tile_next = n_tiles > 0 ? cur.next() : -1;   // key tile of the next iteration
         uint4 mw = make_uint4(~0u, ~0u, ~0u, ~0u);
-        if (MASK && row_masked && n_tiles > 0) mw = __ldg(reinterpret_cast<const uint4*>(mrow) + tile_next);
+        // (debug library) the four words of a key tile lie inside the mask's extent
+        auto mask_ok = [&](int tile) {
+            const int64_t w0 = static_cast<int64_t>(b) * a.mask_sb + static_cast<int64_t>(row) * a.mask_si + 4 * tile;
+            return in_bounds(tile >= 0 && w0 >= 0 && w0 + 4 <= a.dbg_mask_words, a.status, ROLE_SOFTMAX, BND_MASK);
+        };
+        if (MASK && row_masked && n_tiles > 0 && mask_ok(tile_next))
+            mw = __ldg(reinterpret_cast<const uint4*>(mrow) + tile_next);
         // offset used in the exponent: 0 while no key of the row has been seen
         auto m_off = [&](float mm) { return (MASK && mm == -INFINITY) ? 0.f : mm; };
 
@@ -430,7 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_next = j + 1 < n_tiles ? cur.next() : -1;
             const int valid = a.kv_len - tile * kBN;   // >= 1
             uint4 mcur = mw;
-            if (MASK && row_masked && j + 1 < n_tiles) mw = __ldg(reinterpret_cast<const uint4*>(mrow) + tile_next);
+            if (MASK && row_masked && j + 1 < n_tiles && mask_ok(tile_next))
+                mw = __ldg(reinterpret_cast<const uint4*>(mrow) + tile_next);
             float s[128];
 #pragma unroll
             for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
@@ -512,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar(C::kPFull + t));
+            if (!(warp == 0 && inject(a, FAULT_SKIP_P_ARRIVE, j))) mbar_arrive(bar(C::kPFull + t));
         }
 
         // ---------------------------------------------------------------- epilogue
@@ -534,7 +563,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (ACCUM) {
                 // Merge with the pass already in (out, lse): the same combine as
                 // dit_attn_lse_merge, for two partials.
-                const float lse_prev = in_range ? a.lse[lse_idx] : -INFINITY;
+                const float lse_prev =
+                    (in_range && in_bounds(lse_idx >= 0 && lse_idx < static_cast<int64_t>(a.B) * a.H * a.Nq, a.status,
+                                           ROLE_SOFTMAX, BND_LSE))
+                        ? a.lse[lse_idx]
+                        : -INFINITY;
                 const float mx = fmaxf(lse_prev, lse_new);
                 if (mx == -INFINITY) {
                     c_new = 0.f;
@@ -583,11 +616,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int grow = q_row0 + t * kBM + wq * 32 + r;
                     if (PIECE && grow < a.Nq) {
                         // a piece's fp32 partial, row-major [256][D] in its workspace slot
-                        *reinterpret_cast<float4*>(a.ws_o + (static_cast<int64_t>(blockIdx.x) * (2 * kBM) + (grow - q_row0)) * D +
-                                                   cc * 32 + 4 * k4) = val;
+                        const int64_t wi = (static_cast<int64_t>(blockIdx.x) * (2 * kBM) + (grow - q_row0)) * D + cc * 32 + 4 * k4;
+                        if (in_bounds(wi >= 0 && wi + 4 <= static_cast<int64_t>(a.n_split_ctas) * (2 * kBM) * D, a.status,
+                                      ROLE_SOFTMAX, BND_WS))
+                            *reinterpret_cast<float4*>(a.ws_o + wi) = val;
                     } else if (grow < a.Nq) {
                         const int64_t off = static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(grow) * a.o_sn +
                                             static_cast<int64_t>(h) * a.o_sh + cc * 32 + 4 * k4;
+                        if (!in_bounds(off >= 0 && off + 4 <= a.dbg_o_elems, a.status, ROLE_SOFTMAX, BND_OUT)) continue;
                         if constexpr (OUT_BF16) {
                             *reinterpret_cast<uint2*>(out_h + off) =
                                 make_uint2(pack_bf16x2(val.x, val.y), pack_bf16x2(val.z, val.w));
@@ -607,10 +643,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
             if (in_range) {
-                if (PIECE)
-                    a.ws_lse[static_cast<int64_t>(blockIdx.x) * (2 * kBM) + (row - q_row0)] = lse_out;
-                else
+                if (PIECE) {
+                    const int64_t wi = static_cast<int64_t>(blockIdx.x) * (2 * kBM) + (row - q_row0);
+                    if (in_bounds(wi >= 0 && wi < static_cast<int64_t>(a.n_split_ctas) * (2 * kBM), a.status,
+                                  ROLE_SOFTMAX, BND_WS))
+                        a.ws_lse[wi] = lse_out;
+                } else if (in_bounds(lse_idx >= 0 && lse_idx < static_cast<int64_t>(a.B) * a.H * a.Nq, a.status,
+                                     ROLE_SOFTMAX, BND_LSE)) {
                     a.lse[lse_idx] = lse_out;
+                }
             }
         }
     }
@@ -679,6 +720,11 @@ __global__ void __launch_bounds__(256) attn_tail_merge_kernel(const AttnArgs a) 
     const int grow = qblk * (2 * kBM) + r;
     if (grow >= a.Nq) return;
     const int64_t piece0 = static_cast<int64_t>(it) * f;
+    // (debug library) the item, its pieces' partials and the output lie in bounds
+    const int64_t n_ws_rows = static_cast<int64_t>(a.n_split_ctas) * (2 * kBM);
+    if (!in_bounds(h < a.H && b < a.B && f >= 1 && f <= kMaxSplit && (piece0 + f) * (2 * kBM) <= n_ws_rows, a.status,
+                   0, BND_WS))
+        return;
     float lp[kMaxSplit];
     float mx = -INFINITY;
 #pragma unroll
@@ -703,6 +749,7 @@ __global__ void __launch_bounds__(256) attn_tail_merge_kernel(const AttnArgs a) 
     const float inv = 1.f / wsum;
     const int64_t off = static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(grow) * a.o_sn +
                         static_cast<int64_t>(h) * a.o_sh + 4 * c4;
+    if (!in_bounds(off >= 0 && off + 4 <= a.dbg_o_elems, a.status, 0, BND_OUT)) return;
     if constexpr (OUT_BF16) {
         *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + off) =
             make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));

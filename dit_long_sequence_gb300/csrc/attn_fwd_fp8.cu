@@ -30,6 +30,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "debug.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -61,6 +62,7 @@ constexpr int kNumBars = kLoadDrain + 1;
 constexpr int kBarOffset = (2 + kStages) * kTile;
 constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
 static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(256 + 2 * kD <= 512, "S0, S1, O0, O1 fit the 512 TMEM columns");
 
 __device__ __forceinline__ float max64(const float* v) {
     float t8[8];
@@ -118,6 +120,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         if (static_cast<int>(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)) >= a.split_first) return;
     }
+    // (debug library) the item and its key range lie inside the problem
+    if (!in_bounds(h >= 0 && h < a.H && b >= 0 && b < a.B && q_row0 >= 0 && q_row0 < a.Nq && k_begin >= 0 &&
+                       n_tiles >= 0 && k_begin + n_tiles <= a.n_kv_tiles,
+                   a.status, 0, BND_ITEM))
+        return;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(kQFull + 0), 1);
@@ -163,19 +170,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int total = 2 * n_tiles;
             int issued = 0;
+            int withheld = -1;   // (debug library) the load skipped on request
             for (int i = 0; i < total; ++i) {
                 const int slot = i % S;
                 const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
+                const int key0 = (k_begin + (i >> 1)) * kBN;
+                if (!in_bounds(key0 >= 0 && key0 < a.kv_len, a.status, ROLE_LOAD, BND_KEY)) break;
                 if (!wait_bounded(bar(kKVEmpty + slot), ph ^ 1u, wd, ROLE_LOAD, SITE_KV_EMPTY)) break;
-                mbar_arrive_expect_tx(bar(kKVFull + slot), kTile);
-                tma_load_4d(sRing + slot * kTile, (i & 1) ? &tm_v : &tm_k, bar(kKVFull + slot), 0,
-                            (k_begin + (i >> 1)) * kBN, h, b);
                 issued = i + 1;
+                if (inject(a, FAULT_SKIP_LOAD, i)) {
+                    withheld = i;   // neither the arrive nor the copy: the slot never fills
+                    continue;
+                }
+                mbar_arrive_expect_tx(bar(kKVFull + slot), kTile);
+                tma_load_4d(sRing + slot * kTile, (i & 1) ? &tm_v : &tm_k, bar(kKVFull + slot), 0, key0, h, b);
             }
             if (issued < total || *abort_flag) {
                 for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
-                    wait_bounded(bar(kKVFull + i % S), static_cast<uint32_t>(i / S) & 1u, wd_drain, ROLE_LOAD,
-                                 SITE_LOAD_DRAIN);
+                    if (i != withheld)
+                        wait_bounded(bar(kKVFull + i % S), static_cast<uint32_t>(i / S) & 1u, wd_drain, ROLE_LOAD,
+                                     SITE_LOAD_DRAIN);
                 wait_bounded(bar(kQFull + 0), 0, wd_drain, ROLE_LOAD, SITE_LOAD_DRAIN);
                 wait_bounded(bar(kQFull + 1), 0, wd_drain, ROLE_LOAD, SITE_LOAD_DRAIN);
             }
@@ -209,10 +223,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = wait_bounded(bar(kQFull + 0), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
                       wait_bounded(bar(kQFull + 1), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
                       wait_bounded(bar(kKVFull + 0), 0, wd, ROLE_MMA, SITE_KV_FULL);
+            // S_0 number n is ready (the debug library can withhold one signal)
+            auto commit_s0 = [&](int n) {
+                if (!inject(a, FAULT_SKIP_S_COMMIT, n)) umma_commit(bar(kSFull + 0));
+            };
             if (ok) {
                 tc_fence_after();
                 issue_qk(tS0, sQ, sRing);
-                umma_commit(bar(kSFull + 0));
+                commit_s0(0);
                 issue_qk(tS1, sQ + kTile, sRing);
                 umma_commit(bar(kSFull + 1));
                 umma_commit(bar(kKVEmpty + 0));
@@ -223,6 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t k_addr = sRing + (ik % S) * kTile;
                 const bool more = j + 1 < n_tiles;
                 const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+                if (!in_bounds(v_addr >= sRing && v_addr + kTile <= sRing + S * kTile && k_addr >= sRing &&
+                                   k_addr + kTile <= sRing + S * kTile,
+                               a.status, ROLE_MMA, BND_SMEM))
+                    break;
                 ok = wait_bounded(bar(kKVFull + iv % S), static_cast<uint32_t>(iv / S) & 1u, wd, ROLE_MMA,
                                   SITE_KV_FULL) &&
                      wait_bounded(bar(kPFull + 0), ph, wd, ROLE_MMA, SITE_P_FULL);
@@ -235,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     tc_fence_after();
                     issue_qk(tS0, sQ, k_addr);
-                    umma_commit(bar(kSFull + 0));
+                    commit_s0(j + 1);
                 } else {
                     umma_commit(bar(kOFinal + 0));
                 }
@@ -337,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             l += exp_store(s, tS, neg) + exp_store(s + 64, tS + 16, neg);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar(kPFull + t));
+            if (!(warp == 0 && inject(a, FAULT_SKIP_P_ARRIVE, j))) mbar_arrive(bar(kPFull + t));
         }
 
         // ---------------------------------------------------------------- epilogue
@@ -380,11 +402,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int grow = q_row0 + t * kBM + wq * 32 + r;
                     if (PIECE && grow < a.Nq) {
                         // a piece's fp32 partial, row-major [256][D] in its workspace slot
-                        *reinterpret_cast<float4*>(a.ws_o + (static_cast<int64_t>(blockIdx.x) * (2 * kBM) + (grow - q_row0)) * kD +
-                                                   cc * 32 + 4 * k4) = val;
+                        const int64_t wi = (static_cast<int64_t>(blockIdx.x) * (2 * kBM) + (grow - q_row0)) * kD + cc * 32 + 4 * k4;
+                        if (in_bounds(wi >= 0 && wi + 4 <= static_cast<int64_t>(a.n_split_ctas) * (2 * kBM) * kD, a.status,
+                                      ROLE_SOFTMAX, BND_WS))
+                            *reinterpret_cast<float4*>(a.ws_o + wi) = val;
                     } else if (grow < a.Nq) {
                         const int64_t off = static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(grow) * a.o_sn +
                                             static_cast<int64_t>(h) * a.o_sh + cc * 32 + 4 * k4;
+                        if (!in_bounds(off >= 0 && off + 4 <= a.dbg_o_elems, a.status, ROLE_SOFTMAX, BND_OUT)) continue;
                         if constexpr (OUT_BF16)
                             *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + off) =
                                 make_uint2(pack_bf16x2(val.x, val.y), pack_bf16x2(val.z, val.w));
@@ -396,10 +421,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float lse_out = n_tiles > 0 ? (m - kPOffset + log2f(l)) * kLn2 : -INFINITY;
             if (in_range) {
-                if (PIECE)
-                    a.ws_lse[static_cast<int64_t>(blockIdx.x) * (2 * kBM) + (row - q_row0)] = lse_out;
-                else
+                if (PIECE) {
+                    const int64_t wi = static_cast<int64_t>(blockIdx.x) * (2 * kBM) + (row - q_row0);
+                    if (in_bounds(wi >= 0 && wi < static_cast<int64_t>(a.n_split_ctas) * (2 * kBM), a.status,
+                                  ROLE_SOFTMAX, BND_WS))
+                        a.ws_lse[wi] = lse_out;
+                } else if (in_bounds(lse_idx >= 0 && lse_idx < static_cast<int64_t>(a.B) * a.H * a.Nq, a.status,
+                                     ROLE_SOFTMAX, BND_LSE)) {
                     a.lse[lse_idx] = lse_out;
+                }
             }
         }
     }

@@ -14,6 +14,24 @@ enum WatchSite : uint32_t {
     SITE_Q_FULL = 1, SITE_KV_FULL = 2, SITE_KV_EMPTY = 3, SITE_S_FULL = 4, SITE_P_FULL = 5,
     SITE_O_FINAL = 6, SITE_DRAIN = 7, SITE_LOAD_DRAIN = 8
 };
+// Sites of the debug library's bounds checks (status word 3 with code 6).
+enum BoundSite : uint32_t {
+    BND_ITEM = 101,   // work item decoded outside (B, H, Nq)
+    BND_KEY = 102,    // key tile outside [0, kv_len)
+    BND_SMEM = 103,   // shared-memory operand or staging address outside its buffer
+    BND_TMEM = 104,   // tensor-memory column outside the 512 allocated
+    BND_OUT = 105,    // O element outside the extent its strides reach
+    BND_LSE = 106,    // LSE element outside [B, H, Nq]
+    BND_WS = 107,     // workspace element outside the split pieces' partials
+    BND_MASK = 108,   // mask word outside the extent its strides reach
+};
+// Faults the debug library can inject (one withheld producer signal).
+enum DebugFault : uint32_t {
+    FAULT_NONE = 0,
+    FAULT_SKIP_LOAD = 1,       // the TMA thread skips K/V load `index` (no arrive, no copy)
+    FAULT_SKIP_S_COMMIT = 2,   // the MMA thread skips the completion signal of S_0 number `index`
+    FAULT_SKIP_P_ARRIVE = 3,   // softmax warp 0 skips its P-ready arrive at key tile `index`
+};
 
 struct AttnArgs {
     int Nq;            // query rows
@@ -46,6 +64,14 @@ struct AttnArgs {
     int n_split_ctas;          // (items - split_first) * split_f
     float* ws_o;
     float* ws_lse;
+    int B;                     // batch count
+    // Debug library only (zero in the product library): one injected fault
+    // and the extents the in-kernel bounds checks compare against.
+    uint32_t dbg_fault;        // DebugFault
+    int dbg_fault_cta;         // linear block index of the CTA that injects it
+    int dbg_fault_index;       // which load / commit / arrive is withheld
+    int64_t dbg_o_elems;       // O elements reachable through its strides
+    int64_t dbg_mask_words;    // mask words reachable through its strides
 };
 
 // Most pieces one split item is cut into (the tail merge kernel's unrolled

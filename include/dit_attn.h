@@ -62,7 +62,9 @@ typedef enum {
     DIT_ERR_UNSUPPORTED = 2, /* a legal request outside what is built (e.g. D) */
     DIT_ERR_ALIGNMENT = 3,   /* a pointer or stride breaks the 16-byte rules  */
     DIT_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed           */
-    DIT_ERR_TIMEOUT = 5      /* a bounded in-kernel wait ran out (watchdog)   */
+    DIT_ERR_TIMEOUT = 5,     /* a bounded in-kernel wait ran out (watchdog)   */
+    DIT_ERR_BOUNDS = 6       /* an in-kernel bounds check failed (reported by
+                                the debug library only, dit_attn_debug.h)     */
 } dit_status_t;
 
 typedef enum { DIT_BF16 = 0, DIT_F32 = 1 } dit_dtype_t;
@@ -443,7 +445,10 @@ const char *dit_status_string(dit_status_t s);
  * dit_check_watchdog -- synchronise `stream`, read and clear the device
  * status word of the current device.  Returns DIT_OK, DIT_ERR_TIMEOUT (a
  * bounded in-kernel wait ran out; `info`, if non-NULL, receives four words:
- * code, block index, warp role, wait site) or DIT_ERR_CUDA.
+ * code, block index, warp role, wait site), DIT_ERR_BOUNDS (debug library
+ * only: an in-kernel bounds check failed and the access was skipped; `info`
+ * then holds the check's site) or DIT_ERR_CUDA.  Only the first report since
+ * the last read is kept.
  */
 dit_status_t dit_check_watchdog(dit_stream_t stream, uint32_t info[4]);
 

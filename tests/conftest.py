@@ -27,3 +27,16 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _debug_library_status_clean(request):
+    """With the binding on the debug library (DIT_ATTN_DEBUG=1), every GPU
+    test must leave the device status word clean: no bounds check failed and
+    no bounded wait ran out."""
+    yield
+    if os.environ.get("DIT_ATTN_DEBUG") == "1" and "gpu" in request.keywords:
+        from dit_long_sequence_gb300 import binding
+        assert binding.is_debug_library
+        rc, info = binding.check_watchdog()
+        assert rc == 0, f"debug library status {rc} {info} after {request.node.nodeid}"

@@ -41,9 +41,10 @@ def lib():
     return binding
 
 
-def _declared():
-    src = open(os.path.join(ROOT, "include", "dit_attn.h")).read()
-    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(dit_\w+)\s*\(", src, flags=re.M)))
+def _declared(header="dit_attn.h"):
+    src = open(os.path.join(ROOT, "include", header)).read()
+    # declarations start a line with their return type (comment lines start with " *")
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(dit_\w+)\s*\(", src, flags=re.M)))
 
 
 def test_exports_every_declared_symbol(lib):
@@ -54,8 +55,19 @@ def test_exports_every_declared_symbol(lib):
     assert set(lib.EXPORTS) <= set(names)
 
 
+def test_debug_library_exports_both_headers_and_product_none_of_the_debug_calls(lib):
+    dbg = lib.load_debug_library()
+    debug_names = _declared("dit_attn_debug.h")
+    assert set(debug_names) == {"dit_debug_configure", "dit_debug_build"}
+    for n in _declared() + debug_names:
+        assert hasattr(dbg, n), n
+    for n in debug_names:
+        assert not hasattr(lib.raw(), n), n
+    assert dbg.dit_debug_build() == 1
+
+
 def test_status_strings(lib):
-    for s in range(6):
+    for s in range(7):
         assert lib.raw().dit_status_string(s).startswith(b"DIT_")
     assert lib.raw().dit_version() >= 1
 
