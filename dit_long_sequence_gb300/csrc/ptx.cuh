@@ -98,26 +98,6 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Watc
     }
 }
 
-// Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32) of
-// whole warps; every thread of those warps must reach it.
-__device__ __forceinline__ void bar_sync_named(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// The same barrier, returning the OR of `pred` over the participating threads.
-__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t nthreads, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
-        : "memory");
-    return r != 0;
-}
-
 // Per-warp register budget change (whole warpgroup executes it).
 template <uint32_t N>
 __device__ __forceinline__ void regs_increase() {
