@@ -5,7 +5,7 @@ The compute path is libditattn.so (hand-written sm_103a CUDA behind a C ABI,
 the package does not load the library; the first use of an operation does, and
 fails loudly if the library has not been built.
 """
-__all__ = ["attn_fwd", "attn_fwd_ws", "attn_fwd_workspace_bytes", "attn_fwd_masked", "attn_fwd_masked_noalloc", "masked_workspace_bytes", "attn_fwd_accumulate", "lse_merge", "qkv_to_head_major", "qkv_norm_rope_to_head_major",
+__all__ = ["attn_fwd", "attn_fwd_ws", "attn_fwd_workspace_bytes", "attn_fwd_masked", "attn_fwd_masked_noalloc", "masked_workspace_bytes", "masked_split_workspace_bytes", "attn_fwd_accumulate", "lse_merge", "qkv_to_head_major", "qkv_norm_rope_to_head_major",
            "qkv_cast_fp8", "attn_fwd_fp8", "attn_fwd_fp8_ws",
            "split_stacked_fp8", "check_watchdog", "watchdog_selftest", "DitError", "library_path"]
 

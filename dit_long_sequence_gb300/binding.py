@@ -68,6 +68,8 @@ def _declare(lib):
                                                  _i64, _i64, _i, _f, _vp, _i, _vp, _vp]
     lib.dit_attn_masked_workspace_bytes.restype = ctypes.c_size_t
     lib.dit_attn_masked_workspace_bytes.argtypes = [_i, _i, _i]
+    lib.dit_attn_masked_split_workspace_bytes.restype = ctypes.c_size_t
+    lib.dit_attn_masked_split_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
     lib.dit_attn_fwd_fp8.restype = _i
     lib.dit_attn_fwd_fp8.argtypes = [_vp, _vp, _vp, ctypes.POINTER(AttnStrides), _i, _i, _i, _i, _i, _i, _f, _f, _f, _f,
                                       _vp, _i, _vp, _vp]
@@ -111,6 +113,7 @@ def load_debug_library():
 
 
 EXPORTS = ("dit_attn_fwd", "dit_attn_fwd_ws", "dit_attn_fwd_workspace_bytes", "dit_attn_fwd_masked", "dit_attn_fwd_masked_noalloc", "dit_attn_masked_workspace_bytes",
+           "dit_attn_masked_split_workspace_bytes",
            "dit_attn_fwd_accumulate", "dit_attn_lse_merge", "dit_qkv_to_head_major",
            "dit_qkv_norm_rope_to_head_major", "dit_qkv_cast_fp8", "dit_attn_fwd_fp8", "dit_attn_fwd_fp8_ws", "dit_status_string",
            "dit_check_watchdog",
@@ -210,6 +213,12 @@ def masked_workspace_bytes(B: int, Nq: int, key_valid_len: int) -> int:
     return int(_lib.dit_attn_masked_workspace_bytes(int(B), int(Nq), int(key_valid_len)))
 
 
+def masked_split_workspace_bytes(B: int, Nq: int, H: int, D: int, key_valid_len: int) -> int:
+    """Workspace that lets attn_fwd_masked skip empty key tiles and split the
+    grid's last partial wave (current device)."""
+    return int(_lib.dit_attn_masked_split_workspace_bytes(int(B), int(Nq), int(H), int(D), int(key_valid_len)))
+
+
 def attn_fwd_masked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_bits: torch.Tensor, *,
                     mask_rows: int | None = None, key_valid_len: int | None = None, scale: float | None = None,
                     out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
@@ -221,8 +230,10 @@ def attn_fwd_masked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_bits
     j>>5 of row i: query i may attend key j), W a multiple of 4 with
     W >= 4*ceil(key_valid_len/128); a leading dimension of 1 shares the mask
     across the batch.  Rows i >= mask_rows (default R) attend every valid key.
-    With skip_empty_tiles (default) a workspace (allocated here unless given)
-    lets the kernel skip key tiles the mask leaves empty.
+    With skip_empty_tiles (default) a workspace (allocated here unless given,
+    of masked_split_workspace_bytes) lets the kernel skip key tiles the mask
+    leaves empty and split the grid's last partial wave over key ranges; a
+    given workspace of only masked_workspace_bytes skips without splitting.
     """
     B, Nq, H, D = q.shape
     Nkv = k.shape[1]
@@ -251,7 +262,7 @@ def attn_fwd_masked(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask_bits
     sb = 0 if mask_bits.shape[0] == 1 else mask_bits.stride(0)
     ws_ptr, ws_bytes = None, 0
     if skip_empty_tiles:
-        need = masked_workspace_bytes(B, Nq, kvl)
+        need = masked_split_workspace_bytes(B, Nq, H, D, kvl)
         if workspace is None and need > 0:
             workspace = torch.empty((need + 15) // 16 * 16, dtype=torch.uint8, device=q.device)
         if workspace is not None:

@@ -197,6 +197,9 @@ int64_t occ_words_of(int key_valid_len) { return ((key_valid_len + 127) / 128 + 
 int64_t occ_bytes_of(int B, int Nq, int key_valid_len) {
     return static_cast<int64_t>(B) * ((Nq + 255) / 256) * occ_words_of(key_valid_len) * 4;
 }
+// A masked call's workspace: the occupancy map, then (from this offset) the
+// tail split's partials.
+int64_t occ_region_of(int B, int Nq, int key_valid_len) { return (occ_bytes_of(B, Nq, key_valid_len) + 255) / 256 * 256; }
 
 // fp8: E4M3 inputs (D = 128 only), descales[3] = (q, k, v); otherwise bf16.
 // mask: the general bit mask of dit_attn_fwd_masked (bf16 only).
@@ -204,7 +207,7 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
                              int Nq, int Nkv, int H, int D, int key_valid_len, float scale, void* out,
                              dit_dtype_t out_dtype, float* lse, bool accumulate, dit_stream_t stream,
                              const float* descales = nullptr, const MaskSpec* mask = nullptr,
-                             void* workspace = nullptr, size_t workspace_bytes = 0) {
+                             void* workspace = nullptr, size_t workspace_bytes = 0, bool split_optional = false) {
     const bool fp8 = descales != nullptr;
     if (strides == nullptr) return DIT_ERR_INVALID_ARG;
     if (B < 0 || Nq < 0 || Nkv < 0 || H < 0) return DIT_ERR_INVALID_ARG;
@@ -259,9 +262,12 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
     // when the caller gave a workspace for it (plain, unmasked, overwrite only).
     const int64_t items = static_cast<int64_t>(B) * H * ((static_cast<int64_t>(Nq) + 255) / 256);
     SplitPlan split{items, 1, 0};
-    if (workspace != nullptr && !accumulate && mask == nullptr && any_keys) {
+    if (workspace != nullptr && !accumulate && any_keys) {
         split = plan_tail_split(items, (key_valid_len + 127) / 128, device_sm_count(dev));
-        if (workspace_bytes < static_cast<size_t>(split_workspace_bytes(split, D))) return DIT_ERR_INVALID_ARG;
+        if (workspace_bytes < static_cast<size_t>(split_workspace_bytes(split, D))) {
+            if (!split_optional) return DIT_ERR_INVALID_ARG;
+            split = SplitPlan{items, 1, 0};   // a masked call's workspace without room for the split
+        }
         if (!aligned16(workspace)) return DIT_ERR_ALIGNMENT;
     }
     AttnArgs a;
@@ -399,8 +405,26 @@ dit_status_t dit_attn_fwd_masked(const void* q, const void* k, const void* v, co
         if (mask_row_stride % 4 || mask_batch_stride % 4 || !aligned16(mask)) return DIT_ERR_ALIGNMENT;
     }
     const MaskSpec spec{mask, mask_batch_stride, mask_row_stride, mask_rows, static_cast<uint32_t*>(workspace)};
+    // Beyond the occupancy map, room for the tail split's partials (if any) lets
+    // the call split the grid's last partial wave as dit_attn_fwd_ws does.
+    void* split_ws = nullptr;
+    size_t split_bytes = 0;
+    if (workspace != nullptr && B > 0 && Nq > 0 && key_valid_len > 0) {
+        const int64_t region = occ_region_of(B, Nq, key_valid_len);
+        if (workspace_bytes > static_cast<size_t>(region)) {
+            split_ws = static_cast<uint8_t*>(workspace) + region;
+            split_bytes = workspace_bytes - static_cast<size_t>(region);
+        }
+    }
     return attn_fwd_common(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, scale, out, out_dtype, lse, false,
-                           stream, nullptr, &spec);
+                           stream, nullptr, &spec, split_ws, split_bytes, true);
+}
+
+size_t dit_attn_masked_split_workspace_bytes(int B, int Nq, int H, int D, int key_valid_len) {
+    if (B <= 0 || Nq <= 0 || H <= 0 || key_valid_len <= 0 || (D != 64 && D != 128)) return 0;
+    const size_t split = dit_attn_fwd_workspace_bytes(B, Nq, H, D, key_valid_len);
+    if (split == 0) return static_cast<size_t>(occ_bytes_of(B, Nq, key_valid_len));
+    return static_cast<size_t>(occ_region_of(B, Nq, key_valid_len)) + split;
 }
 
 dit_status_t dit_attn_fwd_masked_noalloc(const void* q, const void* k, const void* v,
@@ -414,9 +438,10 @@ dit_status_t dit_attn_fwd_masked_noalloc(const void* q, const void* k, const voi
     if (cudaGetDevice(&dev) != cudaSuccess) return DIT_ERR_CUDA;
     uint32_t* scratch = noalloc_scratch(dev);
     if (scratch == nullptr) return DIT_ERR_CUDA;
+    // exactly the occupancy map's bytes: the fixed array never holds split partials
     return dit_attn_fwd_masked(q, k, v, strides, B, Nq, Nkv, H, D, key_valid_len, mask, mask_batch_stride,
                                mask_row_stride, mask_rows, scale, out, out_dtype, lse, scratch,
-                               static_cast<size_t>(kNoAllocOccWords * 4), stream);
+                               static_cast<size_t>(need > 0 ? need : 16), stream);
 }
 
 dit_status_t dit_attn_fwd_fp8(const void* q, const void* k, const void* v, const dit_attn_strides_t* strides,

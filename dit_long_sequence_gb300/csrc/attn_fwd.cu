@@ -81,15 +81,17 @@
 namespace dit {
 namespace {
 
-// Walks the set bits of one CTA's occupancy words (the key tiles to process);
-// without a map every tile is occupied.
+// Walks the set bits of one CTA's occupancy words in [begin, end) (the key
+// tiles to process; begin < end when there is a map); without a map every
+// tile is occupied.
 struct TileCursor {
-    const uint32_t* words;   // nullptr: all n tiles
+    const uint32_t* words;   // nullptr: all tiles of the range
     int n_words, n, w;
     uint32_t bits;
     int next_all;
     __device__ TileCursor(const uint32_t* occ, int begin, int end)
-        : words(occ), n_words((end + 31) / 32), n(end), w(0), bits(occ ? occ[0] : 0u), next_all(begin) {}
+        : words(occ), n_words((end + 31) / 32), n(end), w(begin >> 5),
+          bits(occ ? occ[begin >> 5] & (~0u << (begin & 31)) : 0u), next_all(begin) {}
     // The next key tile to process, or -1.
     __device__ int next() {
         if (words == nullptr) return next_all < n ? next_all++ : -1;
@@ -103,10 +105,16 @@ struct TileCursor {
     }
 };
 
-__device__ __forceinline__ int count_tiles(const uint32_t* occ, int n_tiles) {
-    if (occ == nullptr) return n_tiles;
+// Occupied key tiles in [begin, end) (all of them without a map).
+__device__ __forceinline__ int count_tiles(const uint32_t* occ, int begin, int end) {
+    if (occ == nullptr) return end - begin;
     int c = 0;
-    for (int w = 0; w < (n_tiles + 31) / 32; ++w) c += __popc(occ[w]);
+    for (int w = begin >> 5; w < (end + 31) >> 5; ++w) {
+        uint32_t bits = occ[w];
+        if (w == (begin >> 5)) bits &= ~0u << (begin & 31);
+        if (w == ((end - 1) >> 5) && (end & 31) != 0) bits &= (1u << (end & 31)) - 1u;
+        c += __popc(bits);
+    }
     return c;
 }
 
@@ -168,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Work item of this CTA: (256-row block, head, batch) = (x, y, z) for a
     // whole item; a piece decodes its item and key range from its 1-D index
     // (items counted block fastest, then head, then batch).
-    static_assert(!PIECE || (!ACCUM && !MASK), "only plain overwriting passes are split");
+    static_assert(!PIECE || !ACCUM, "only overwriting passes are split");
     struct W { int h, b, q_row0, qblk; };
     int k_begin = 0, k_end = a.n_kv_tiles;   // key tiles [k_begin, k_end) of this CTA
     auto item_w = [&]() {
@@ -199,17 +207,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                        k_begin <= k_end && k_end <= a.n_kv_tiles,
                    a.status, 0, BND_ITEM))
         return;
-    if constexpr (!PIECE && !ACCUM && !MASK) {
+    if constexpr (!PIECE && !ACCUM) {
         // The piece kernel (if any) may start once every CTA here has begun;
         // the items it covers are the last in grid order and left to it.
         if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         if (static_cast<int>(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)) >= a.split_first) return;
     }
-    // MASK with an occupancy map: this CTA's row of tile bits
+    // MASK with an occupancy map: this item's row of tile bits
     const uint32_t* occ = (MASK && a.occ != nullptr)
-                              ? a.occ + (static_cast<int64_t>(b) * gridDim.x + blockIdx.x) * a.occ_words
+                              ? a.occ + (static_cast<int64_t>(b) * a.n_qblk + wk.qblk) * a.occ_words
                               : nullptr;
-    const int n_tiles = PIECE ? k_end - k_begin : count_tiles(occ, a.n_kv_tiles);   // key tiles this CTA processes
+    const int n_tiles = count_tiles(occ, k_begin, k_end);   // key tiles this CTA processes
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::kQFull + 0), 1);
@@ -678,10 +686,10 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     const dim3 grid(args.n_qblk, args.H, B);
     kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, args);
     e = cudaGetLastError();
-    if (e != cudaSuccess || ACCUM || MASK || args.n_split_ctas == 0) return e;
+    if (e != cudaSuccess || ACCUM || args.n_split_ctas == 0) return e;
     // The split items' pieces: a programmatic dependent launch, so that its
     // CTAs take SMs as the last whole items drain instead of after the grid.
-    auto piece = attn_fwd_kernel<D, BF16, false, false, true>;
+    auto piece = attn_fwd_kernel<D, BF16, false, MASK, true>;
     e = cudaFuncSetAttribute(piece, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -699,10 +707,11 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 
 // Combine the split pieces: per (split item, row) the f normalised partials
 // (O_p, LSE_p) give O = sum_p w_p O_p, LSE = M + ln sum_p e^(LSE_p - M), with
-// w_p = e^(LSE_p - M) / sum_q e^(LSE_q - M) and M = max_p LSE_p.  Every piece
-// covers at least one valid key, so each LSE_p is finite.  D/4 lanes per row,
-// one float4 of O each: coalesced reads of the row-major partials and of the
-// output row.
+// w_p = e^(LSE_p - M) / sum_q e^(LSE_q - M) and M = max_p LSE_p.  A piece whose
+// range holds no key the row may attend (general mask) has LSE_p = -inf and
+// weight 0; a row with none in any piece gets O = 0, LSE = -inf.  D/4 lanes per
+// row, one float4 of O each: coalesced reads of the row-major partials and of
+// the output row.
 template <int D, bool OUT_BF16>
 __global__ void __launch_bounds__(256) attn_tail_merge_kernel(const AttnArgs a) {
     constexpr int LPR = D / 4;
@@ -734,9 +743,11 @@ __global__ void __launch_bounds__(256) attn_tail_merge_kernel(const AttnArgs a) 
     }
     float wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // A masked row may have no allowed key in some pieces (LSE -inf, weight 0)
+    // or in all of them (O = 0, LSE = -inf).
 #pragma unroll
     for (int p = 0; p < kMaxSplit; ++p) {
-        if (p < f) {
+        if (p < f && mx != -INFINITY) {
             const float w = expf(lp[p] - mx);
             wsum += w;
             const float4 o = __ldcs(reinterpret_cast<const float4*>(a.ws_o + ((piece0 + p) * (2 * kBM) + r) * D) + c4);
@@ -746,7 +757,7 @@ __global__ void __launch_bounds__(256) attn_tail_merge_kernel(const AttnArgs a) 
             acc.w = fmaf(w, o.w, acc.w);
         }
     }
-    const float inv = 1.f / wsum;
+    const float inv = mx != -INFINITY ? 1.f / wsum : 0.f;
     const int64_t off = static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(grow) * a.o_sn +
                         static_cast<int64_t>(h) * a.o_sh + 4 * c4;
     if (!in_bounds(off >= 0 && off + 4 <= a.dbg_o_elems, a.status, 0, BND_OUT)) return;
@@ -757,7 +768,7 @@ __global__ void __launch_bounds__(256) attn_tail_merge_kernel(const AttnArgs a) 
         *reinterpret_cast<float4*>(static_cast<float*>(a.out) + off) =
             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
-    if (c4 == 0) a.lse[(static_cast<int64_t>(b) * a.H + h) * a.Nq + grow] = mx + logf(wsum);
+    if (c4 == 0) a.lse[(static_cast<int64_t>(b) * a.H + h) * a.Nq + grow] = mx != -INFINITY ? mx + logf(wsum) : -INFINITY;
 }
 
 }  // namespace

@@ -199,6 +199,11 @@ size_t dit_attn_fwd_workspace_bytes(int B, int Nq, int H, int D, int key_valid_l
  *        128-key tiles each 256-row query block attends at all, and the
  *        attention then loads and multiplies only those (block-local masks
  *        skip most tiles).  NULL processes every tile (same results).
+ *        With dit_attn_masked_split_workspace_bytes or more, the space past
+ *        the occupancy map (which starts the workspace, rounded up to 256
+ *        bytes) also holds the tail split of dit_attn_fwd_ws: the grid's last
+ *        partial wave runs as key-range pieces, merged exactly.  A smaller
+ *        workspace is not an error; the call then runs unsplit.
  * Other arguments as dit_attn_fwd.
  */
 dit_status_t dit_attn_fwd_masked(const void *q, const void *k, const void *v,
@@ -238,6 +243,17 @@ dit_status_t dit_attn_fwd_masked_noalloc(const void *q, const void *k, const voi
                                          int64_t mask_row_stride, int mask_rows,
                                          float scale, void *out, dit_dtype_t out_dtype, float *lse,
                                          dit_stream_t stream);
+
+/*
+ * dit_attn_masked_split_workspace_bytes -- bytes of `workspace` that let
+ * dit_attn_fwd_masked both skip empty key tiles and split the grid's last
+ * partial wave (the occupancy map rounded up to 256 bytes, then the split's
+ * partials, dit_attn_fwd_workspace_bytes of them); the bare occupancy map's
+ * size when no split helps.  Like dit_attn_fwd_workspace_bytes, the size holds
+ * for the device current at query time (its SM count sets the split).  0 when
+ * there is nothing to compute or D is not 64 or 128.  Host only.
+ */
+size_t dit_attn_masked_split_workspace_bytes(int B, int Nq, int H, int D, int key_valid_len);
 
 /*
  * dit_attn_masked_workspace_bytes -- bytes of `workspace` that let

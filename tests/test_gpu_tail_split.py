@@ -354,3 +354,74 @@ def test_split_reruns_are_bit_identical(fp8):
     torch.cuda.synchronize()
     assert dl.attn_fwd_workspace_bytes(B, N, H, D, kvl) > 0
     assert torch.equal(O1, O2) and torch.equal(L1, L2)
+
+
+# ------------------------------------------------------------ general mask
+# dit_attn_fwd_masked splits the grid's last partial wave as dit_attn_fwd_ws
+# does when its workspace has room past the occupancy map.  A piece's key
+# range may hold no key a row may attend: its partial then has LSE = -inf and
+# weight 0 in the merge, and a row with none in any piece ends with O = 0,
+# LSE = -inf.
+
+def _masked_oracle(q, k, v, m, T, Tp):
+    import oracle
+    return oracle.attn(parity.host_bits(q), parity.host_bits(k), parity.host_bits(v), key_valid_len=T,
+                       allow=oracle.expand_mask(m.numpy(), Tp))
+
+
+def _random_mask(B, T, density, seed, empty_rows=(), late_rows=()):
+    g = torch.Generator().manual_seed(seed)
+    m = torch.rand((B, T, T), generator=g) < density
+    for bb, ii in empty_rows:
+        m[bb, ii] = False
+    for bb, ii, first_key in late_rows:            # no allowed key before first_key
+        m[bb, ii, :first_key] = False
+    return m
+
+
+@pytest.mark.parametrize("B,T,Tp,H,D,f_152,first_152,seed,kind", [
+    (1, 8000, 8192, 2, 128, 2, 0, 51, "random"),       # 64 items, all split in two
+    (2, 4400, 4500, 2, 128, 2, 0, 52, "random"),       # B = 2, ragged query blocks
+    (1, 4096, 4096, 4, 128, 2, 0, 53, "blocks"),       # block-diagonal: pieces with no allowed key
+    (1, 4096, 4096, 10, 128, 2, 152, 54, "blocks"),    # 160 items: 152 whole, 8 split
+])
+def test_masked_split_matches_oracle_and_unsplit(B, T, Tp, H, D, f_152, first_152, seed, kind):
+    import dit_long_sequence_gb300 as dl
+    q, k, v, _ = wl.make_qkv(B, Tp, H, D, seed, device=_dev())
+    if kind == "random":
+        m = _random_mask(B, T, 0.3, seed, empty_rows=((0, 5), (B - 1, T - 1)),
+                         late_rows=((0, 300, T // 2), (B - 1, 600, T - 10)))
+    else:
+        idx = torch.arange(T)
+        m = ((idx[:, None] // 512) == (idx[None, :] // 512))[None].repeat(B, 1, 1)
+        m[0, 1000] = False                          # one row attends nothing
+    bits = wl.pack_mask_bits(m).to(_dev())
+    f, first = _plan(B, Tp, H, T)
+    if _sms() == 152:
+        assert (f, first) == (f_152, first_152)
+    need = dl.masked_split_workspace_bytes(B, Tp, H, D, T)
+    occ = dl.masked_workspace_bytes(B, Tp, T)
+    assert need == (occ + 255) // 256 * 256 + dl.attn_fwd_workspace_bytes(B, Tp, H, D, T)
+    ws = torch.empty(need, dtype=torch.uint8, device=_dev())
+    O, L = dl.attn_fwd_masked(q, k, v, bits, key_valid_len=T, workspace=ws)
+    ws0 = torch.empty((occ + 15) // 16 * 16, dtype=torch.uint8, device=_dev())   # occupancy only: no split
+    O0, L0 = dl.attn_fwd_masked(q, k, v, bits, key_valid_len=T, workspace=ws0)
+    torch.cuda.synchronize()
+    Or, Lr = _masked_oracle(q, k, v, m, T, Tp)
+    parity.compare(O.double().permute(0, 2, 1, 3).cpu().numpy(), L.double().cpu().numpy(),
+                   Or.transpose(0, 2, 1, 3), Lr)
+    parity.compare(O0.double().permute(0, 2, 1, 3).cpu().numpy(), L0.double().cpu().numpy(),
+                   Or.transpose(0, 2, 1, 3), Lr)
+    assert torch.equal(torch.isneginf(L), torch.isneginf(L0))
+    fin = torch.isfinite(L0)
+    assert (O - O0).abs().max().item() <= SPLIT_VS_SINGLE_O
+    assert (L[fin] - L0[fin]).abs().max().item() <= SPLIT_VS_SINGLE_LSE
+    # items before the split are the unsplit kernel's, bit for bit
+    split_rows = torch.from_numpy(_split_rows_mask(B, Tp, H, T)).to(_dev())   # [B, H, Nq]
+    whole = ~split_rows
+    assert torch.equal(L[whole], L0[whole])
+    assert torch.equal(O.permute(0, 2, 1, 3)[whole], O0.permute(0, 2, 1, 3)[whole])
+    if kind == "blocks":
+        assert torch.all(O[0, 1000] == 0) and torch.all(torch.isneginf(L[0, :, 1000]))
+    rc, info = dl.check_watchdog()
+    assert rc == 0, info
