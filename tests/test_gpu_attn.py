@@ -110,6 +110,49 @@ def test_large_score_jumps_exercise_the_rescale_paths(D):
     parity.compare(O.double().cpu().numpy(), L.double().cpu().numpy(), Or, Lr, head_axes=(0, 2))
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("masked", [False, True])
+def test_score_jumps_by_warp_exercise_every_rescale_order(D, masked):
+    # Each 32-row warp of queries is tied to one of four keys: channel c of
+    # warp w's rows (c = w mod 4) is raised, and key_c carries a large value in
+    # channel c.  Those rows see their scores jump by ~60 in log2 units at key_c,
+    # far past the 2^39 row-sum limit, while the other warps' rows barely move.
+    # key_0 and key_2 sit in the second 64-key half of their tile and key_1 and
+    # key_3 in the first (the softmax takes a tile's scores in two halves), so
+    # the rescale is triggered from either half, in some warps of a query tile
+    # while the others take none.
+    B, N, H = 1, 1024, 2
+    g = wl.generator(_dev(), 22)
+    q = torch.randn(B, N, H, D, generator=g, device=_dev()) * 0.5
+    k = torch.randn(B, N, H, D, generator=g, device=_dev()) * 0.5
+    v = torch.randn(B, N, H, D, generator=g, device=_dev())
+    keys = (200, 300, 470, 530)      # (tile, key within the tile): (1, 72), (2, 44), (3, 86), (4, 18)
+    rows = torch.arange(N, device=_dev())
+    for c, key in enumerate(keys):
+        q[:, (rows // 32) % 4 == c, :, c] += 6.0
+        k[:, key, :, c] += 7.0 * math.sqrt(D)
+    q, k, v = (x.to(torch.bfloat16) for x in (q, k, v))
+    if masked:
+        import dit_long_sequence_gb300 as dl
+        allow = torch.ones((1, N, N), dtype=torch.bool)
+        allow[0, ::7, 100:260] = False       # some rows miss key 200
+        bits = wl.pack_mask_bits(allow).to(_dev())
+        O, L = dl.attn_fwd_masked(q, k, v, bits)
+    else:
+        O, L = _attn(q, k, v)
+    torch.cuda.synchronize()
+    if masked:
+        import oracle
+        Or, Lr = oracle.attn(parity.host_bits(q), parity.host_bits(k), parity.host_bits(v),
+                             allow=oracle.expand_mask(allow.numpy(), N))
+    else:
+        Or, Lr = parity.oracle_full(q, k, v)
+    # the jumps really are large: nearly every row's LSE sits more than 27
+    # (2^39 in log2 units) above the ln N that keys without a jump would give
+    assert np.mean(Lr > np.log(N) + 27.0) > 0.9
+    parity.compare(O.double().cpu().numpy(), L.double().cpu().numpy(), Or, Lr, head_axes=(0, 2))
+
+
 def test_pad_keys_never_read_and_deterministic():
     B, N, H, D, kvl = 1, 700, 2, 128, 515
     q, k, v, _ = wl.make_qkv(B, N, H, D, seed=12, device=_dev())
