@@ -1,6 +1,7 @@
 """Host logic of bench.py, on the CPU: the multi-rank reduction (two gloo ranks),
-the FLOP accounting, clock-sample filtering, the profile-hash gate on the
-reported DRAM traffic, and a bounded CPU-baseline sample."""
+the FLOP accounting, clock-sample filtering, the choice of the roofline's
+peak, the profile-hash gate on the reported DRAM traffic, and a bounded
+CPU-baseline sample."""
 import json
 import math
 import os
@@ -113,6 +114,15 @@ def test_traffic_only_reported_for_the_profiled_kernel_source(tmp_path, monkeypa
     rec["entries"][0]["kernel_source_sha256_16"] = "0000000000000000"
     (prof / "dram_traffic.json").write_text(json.dumps(rec))
     assert bench.profiled_traffic("w") is None
+
+
+def test_peak_is_the_sustained_figure_only_under_the_power_cap():
+    peaks = {"bf16_tflops": 1896.7, "bf16_tflops_sustained": 1693.2}
+    assert bench.choose_bf16_peak(peaks, {"reasons": []}) == (1896.7, "burst")
+    v, kind = bench.choose_bf16_peak(peaks, {"reasons": ["sw_power_cap"]})
+    assert v == 1693.2 and kind.startswith("sustained")
+    assert bench.choose_bf16_peak({"bf16_tflops": 1900.0}, {"reasons": ["sw_power_cap"]})[0] == 1900.0
+    assert bench.choose_bf16_peak(peaks, {"reasons": ["clock sampling unavailable"]})[0] == 1896.7
 
 
 def test_cpu_baseline_is_bounded_and_in_the_metric_unit():
