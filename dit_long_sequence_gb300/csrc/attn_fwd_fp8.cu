@@ -317,25 +317,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
 
+            // The S row with its maximum: each load also reduces its 32 columns.
             uint32_t sr[4][32];
-            tmem_ld32(tS + 0, sr[0]);
-            tmem_ld32(tS + 32, sr[1]);
-            tmem_ld32(tS + 64, sr[2]);
-            tmem_ld32(tS + 96, sr[3]);
+            float pm[4];
+            tmem_ld32_max(tS + 0, sr[0], pm[0]);
+            tmem_ld32_max(tS + 32, sr[1], pm[1]);
+            tmem_ld32_max(tS + 64, sr[2], pm[2]);
+            tmem_ld32_max(tS + 96, sr[3], pm[3]);
             tmem_ld_wait_dep(sr[0]);
             reg_dep(sr[1]);
             reg_dep(sr[2]);
             reg_dep(sr[3]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) reg_dep(pm[i]);
             const int valid = a.kv_len - (k_begin + j) * kBN;   // >= 1
             float s[128];
 #pragma unroll
             for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+            float mx = fmaxf(max3f(pm[0], pm[1], pm[2]), pm[3]);
             if (valid < 128) {
+                // last tile: the columns past the valid keys hold scores of the
+                // zero-filled key rows, so the maximum is taken over the valid ones
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
                     if (c >= valid) s[c] = -INFINITY;
+                mx = fmaxf(max64(s), max64(s + 64));
             }
-            const float mx = fmaxf(max64(s), max64(s + 64)) * sl2;
+            mx *= sl2;
             const bool need = mx > m + kStale;   // always true on the first tile
             if (__any_sync(0xffffffffu, need)) {
                 const float m_new = need ? mx : m;
