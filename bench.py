@@ -412,8 +412,9 @@ def time_masked_attention(step, reps=3):
     (T, T) user masks over the valid tokens -- frame-local blocks of 1,512
     tokens plus ~5% hashed long-range links (no empty key tile), and the
     frame-local blocks alone (most key tiles empty: with and without the
-    occupancy workspace) -- against the unmasked kernel.  TFLOP/s counts the
-    unmasked FLOPs, i.e. it is an equivalent rate."""
+    occupancy workspace) -- against the unmasked kernel, every call with the
+    workspace that also splits the grid's last partial wave.  TFLOP/s counts
+    the unmasked FLOPs, i.e. it is an equivalent rate."""
     import numpy as np
     import torch
     from dit_long_sequence_gb300 import workloads as wl
@@ -432,7 +433,11 @@ def time_masked_attention(step, reps=3):
         r = np.arange(r0, min(T, r0 + 2048), dtype=np.int64)[:, None]
         local[0, r0:r0 + r.shape[0]] = wl.pack_mask_bits(((r // 1512) == (cols[None, :] // 1512))[None]).numpy()[0]
     local_bits = torch.from_numpy(local).to(step.dev)
-    ws = torch.empty(max(16, step.dl.masked_workspace_bytes(w.B, w.N, T)), dtype=torch.uint8, device=step.dev)
+    # the workspace holds the occupancy map and the tail split, as the unmasked call's does
+    ws = torch.empty(max(16, step.dl.masked_split_workspace_bytes(w.B, w.N, w.H, w.D, T)), dtype=torch.uint8,
+                     device=step.dev)
+    ws_u = torch.empty(max(16, step.dl.attn_fwd_workspace_bytes(w.B, w.N, w.H, w.D, T)), dtype=torch.uint8,
+                       device=step.dev)
     q, k, v = step.q, step.k, step.v
     s = step.stream
     out = {}
@@ -443,8 +448,8 @@ def time_masked_attention(step, reps=3):
                      ("masked_frame_local_no_skip", lambda: step.dl.attn_fwd_masked(
                          q, k, v, local_bits, key_valid_len=T, out=step.out, lse=step.lse,
                          skip_empty_tiles=False, stream=s)),
-                     ("unmasked", lambda: step.dl.attn_fwd(q, k, v, key_valid_len=T, out=step.out, lse=step.lse,
-                                                           stream=s))):
+                     ("unmasked", lambda: step.dl.attn_fwd_ws(q, k, v, key_valid_len=T, out=step.out, lse=step.lse,
+                                                              workspace=ws_u, stream=s))):
         fn()
         ts = []
         for _ in range(reps):
