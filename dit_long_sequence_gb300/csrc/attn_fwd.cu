@@ -27,7 +27,7 @@
 // S_t and fed to the PV product as the TMEM A operand.
 //
 // Per KV tile j the MMA thread issues, in order,
-//   PV0(j-1 ... ) and QK0(j+1) once P0(j) is ready, then PV1(j), QK1(j+1) once
+//   PV0(j) and QK0(j+1) once P0(j) is ready, then PV1(j) and QK1(j+1) once
 //   P1(j) is ready -- so the tensor pipe runs one tile's products while the
 //   other tile's softmax runs.  Products issued by one thread execute in order,
 //   which makes writing S_t(j+1) over P_t(j) safe after PV_t(j).
@@ -70,7 +70,10 @@
 // LSE = -inf.  With an occupancy map (one bit per (256-row block, key tile):
 // does any row of the block attend any key of the tile), every role walks only
 // the occupied key tiles -- the TMA producer loads, the MMA thread multiplies
-// and the softmax warps exponentiate nothing else.
+// and the softmax warps exponentiate nothing else.  The masked kernel splits
+// its last partial wave the same way: a piece walks the occupied tiles of its
+// own key range, and a piece whose range holds no key a row may attend gives
+// that row LSE = -inf, i.e. weight 0 in the merge.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
