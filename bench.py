@@ -72,13 +72,39 @@ def choose_bf16_peak(peaks: dict, clocks: dict):
     return float(peaks["bf16_tflops"]), "burst"
 
 
+def code_only(text: str) -> str:
+    """C/C++ source with its comments removed and its whitespace collapsed
+    (string and character literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(main: str = "attn_fwd.cu") -> str:
-    """Hash of the files an attention kernel is compiled from (its .cu, the PTX
-    wrappers and the kernel-argument header); host-only files are left out."""
+    """Hash of the code an attention kernel is compiled from (its .cu, the PTX
+    wrappers, the debug-check helpers and the kernel-argument header), comments
+    and layout left out; host-only files are left out too."""
     h = hashlib.sha256()
-    for fn in (main, "ptx.cuh", "internal.h"):
-        with open(os.path.join(ROOT, "dit_long_sequence_gb300", "csrc", fn), "rb") as f:
-            h.update(f.read())
+    for fn in (main, "ptx.cuh", "debug.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "dit_long_sequence_gb300", "csrc", fn), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

@@ -104,16 +104,29 @@ def test_traffic_only_reported_for_the_profiled_kernel_source(tmp_path, monkeypa
     prof.mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     os.makedirs(tmp_path / "dit_long_sequence_gb300" / "csrc")
-    for fn in ("attn_fwd.cu", "ptx.cuh", "internal.h"):
-        (tmp_path / "dit_long_sequence_gb300" / "csrc" / fn).write_text(fn)
+    for fn in ("attn_fwd.cu", "ptx.cuh", "debug.cuh", "internal.h"):
+        (tmp_path / "dit_long_sequence_gb300" / "csrc" / fn).write_text(f"int {fn.replace('.', '_')};")
     h = bench.kernel_source_hash()
     rec = {"entries": [{"workload": "w", "kernel_source_sha256_16": h, "dram_bytes_per_call": 1.5e9}]}
     (prof / "dram_traffic.json").write_text(json.dumps(rec))
     assert bench.profiled_traffic("w") == 1.5e9
     assert bench.profiled_traffic("other") is None
+    # a comment or a layout change keeps the capture valid; a code change voids it
+    src = tmp_path / "dit_long_sequence_gb300" / "csrc" / "attn_fwd.cu"
+    src.write_text("// a note\nint   attn_fwd_cu; /* more */\n")
+    assert bench.profiled_traffic("w") == 1.5e9
+    src.write_text("int attn_fwd_cu = 1;")
+    assert bench.profiled_traffic("w") is None
+    src.write_text("int attn_fwd_cu;")
     rec["entries"][0]["kernel_source_sha256_16"] = "0000000000000000"
     (prof / "dram_traffic.json").write_text(json.dumps(rec))
     assert bench.profiled_traffic("w") is None
+
+
+def test_code_only_drops_comments_but_keeps_literals():
+    src = 'int a = 1; // x "y"\n/* multi\n line */ const char* s = "p // q /* r */"; char c = \'"\';'
+    assert bench.code_only(src) == 'int a = 1; const char* s = "p // q /* r */"; char c = \'"\';'
+    assert bench.code_only("a  \n\t b") == "a b"
 
 
 def test_peak_is_the_sustained_figure_only_under_the_power_cap():
