@@ -528,11 +528,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // also true for inf / NaN; MASK: a row with no key seen yet (m = -inf)
                 // always takes the slow path, which sets m from this tile's max
                 const bool need = !(lA + lB <= kSumLimit) || (MASK && m == -INFINITY);
-                if (__any_sync(0xffffffffu, need)) {
+                bool slow = __any_sync(0xffffffffu, need);
+                float m_new = m;
+                if (slow) {
+                    const float m_tile = fmaxf(max64(s), max64(s + 64)) * sl2;
+                    m_new = need ? fmaxf(m_tile, m) : m;
+                    // MASK: rows that still have no allowed key keep m = -inf;
+                    // when no row of the warp moves, its O and P stand as they are
+                    if constexpr (MASK) slow = __any_sync(0xffffffffu, m_new != m);
+                }
+                if (slow) {
                     // O holds PV(j-1) already (S(j) was committed after it).
                     tmem_st_wait();
-                    const float m_tile = fmaxf(max64(s), max64(s + 64)) * sl2;
-                    const float m_new = need ? fmaxf(m_tile, m) : m;
                     const float alpha = (MASK && m_new == -INFINITY) ? 1.f : ex2_approx(m - m_new);
                     l *= alpha;
 #pragma unroll
