@@ -10,6 +10,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "dit_attn.h"
@@ -136,6 +137,36 @@ uint32_t* noalloc_scratch(int dev) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Every buffer a kernel will touch must be memory of the current device (or
+// managed memory), and the stream one of the current device's: a host address
+// or another device's memory handed to a TMA copy or a store is refused here,
+// before anything is enqueued, instead of faulting the GPU.  Null entries are
+// skipped (the caller has already decided which buffers are required).
+dit_status_t check_placement(std::initializer_list<const void*> ptrs, dit_stream_t stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DIT_ERR_CUDA;
+    for (const void* p : ptrs) {
+        if (p == nullptr) continue;
+        cudaPointerAttributes at{};
+        if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return DIT_ERR_INVALID_ARG;
+        }
+        const bool here = (at.type == cudaMemoryTypeDevice && at.device == dev) || at.type == cudaMemoryTypeManaged;
+        if (!here) return DIT_ERR_INVALID_ARG;
+    }
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread) {
+        int sdev = -1;
+        if (cudaStreamGetDevice(s, &sdev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return DIT_ERR_INVALID_ARG;
+        }
+        if (sdev != dev) return DIT_ERR_INVALID_ARG;
+    }
+    return DIT_OK;
+}
+
 // A [B, N, H, D] view as a 4-D TMA map (D, N, H, B) with 128-byte swizzle and
 // a box of one swizzle column (64 bf16 or 128 E4M3 channels) by 128 rows.
 // Rows n >= n_rows are outside the map and read as zeros.
@@ -258,6 +289,14 @@ dit_status_t attn_fwd_common(const void* q, const void* k, const void* v, const 
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DIT_ERR_CUDA;
+    {
+        const bool with_mask = mask != nullptr && mask->rows > 0 && any_keys;
+        const dit_status_t st =
+            check_placement({any_keys ? q : nullptr, any_keys ? k : nullptr, any_keys ? v : nullptr, out, lse,
+                             workspace, with_mask ? mask->bits : nullptr, with_mask ? mask->occ : nullptr},
+                            stream);
+        if (st != DIT_OK) return st;
+    }
     // Work items (b, h, 256-row block) of the 1-D bf16 grid, and the tail split
     // when the caller gave a workspace for it (plain, unmasked, overwrite only).
     const int64_t items = static_cast<int64_t>(B) * H * ((static_cast<int64_t>(Nq) + 255) / 256);
@@ -478,6 +517,7 @@ dit_status_t dit_qkv_cast_fp8(const void* qkv, int64_t stride_b, int64_t stride_
     if (stride_b < 0 || stride_n < 0) return DIT_ERR_INVALID_ARG;
     if (stride_b % 8 || stride_n % 8) return DIT_ERR_ALIGNMENT;
     if (!aligned16(qkv) || !aligned16(out)) return DIT_ERR_ALIGNMENT;
+    if (const dit_status_t st = check_placement({qkv, out}, stream); st != DIT_OK) return st;
     CastArgs a;
     a.qkv = static_cast<const uint16_t*>(qkv);
     a.stride_b = stride_b;
@@ -514,6 +554,7 @@ dit_status_t dit_attn_lse_merge(const float* o_parts, int64_t o_chunk_stride, in
     if (!aligned16(o_parts) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse_parts) & 3u) ||
         (reinterpret_cast<uintptr_t>(lse_out) & 3u))
         return DIT_ERR_ALIGNMENT;
+    if (const dit_status_t st = check_placement({o_parts, lse_parts, out, lse_out}, stream); st != DIT_OK) return st;
     MergeArgs a;
     a.o_parts = o_parts;
     a.o_chunk_stride = o_chunk_stride;
@@ -540,6 +581,7 @@ dit_status_t dit_qkv_to_head_major(const void* qkv, int64_t stride_b, int64_t st
     if (stride_b < 0 || stride_n < 0) return DIT_ERR_INVALID_ARG;
     if (stride_b % 8 || stride_n % 8) return DIT_ERR_ALIGNMENT;
     if (!aligned16(qkv) || !aligned16(q_out) || !aligned16(k_out) || !aligned16(v_out)) return DIT_ERR_ALIGNMENT;
+    if (const dit_status_t st = check_placement({qkv, q_out, k_out, v_out}, stream); st != DIT_OK) return st;
     LayoutArgs a;
     a.qkv = static_cast<const uint16_t*>(qkv);
     a.stride_b = stride_b;
@@ -572,6 +614,10 @@ dit_status_t dit_qkv_norm_rope_to_head_major(const void* qkv, int64_t stride_b, 
     if ((q_weight && !aligned16(q_weight)) || (k_weight && !aligned16(k_weight)) ||
         (rope_cos && (!aligned16(rope_cos) || !aligned16(rope_sin))))
         return DIT_ERR_ALIGNMENT;
+    if (const dit_status_t st =
+            check_placement({qkv, q_out, k_out, v_out, q_weight, k_weight, rope_cos, rope_sin}, stream);
+        st != DIT_OK)
+        return st;
     NormRopeArgs a;
     a.qkv = static_cast<const uint16_t*>(qkv);
     a.stride_b = stride_b;

@@ -31,6 +31,11 @@
  *   allocates no memory, copies nothing between host and device and keeps no
  *   per-call state; per-device caches hold kernel attributes, the SM count
  *   and the device addresses of the library's own globals.
+ * - Every buffer a call reads or writes must be memory of the current device
+ *   (cudaMalloc'd, from a memory pool, mapped with the virtual-memory calls,
+ *   or managed memory), and `stream` must belong to the current device.  A
+ *   host pointer (pageable or pinned), another device's memory or another
+ *   device's stream returns DIT_ERR_INVALID_ARG with nothing enqueued.
  * - Strides are in ELEMENTS, not bytes.
  * - Argument, shape, stride and alignment checks run on the host before any
  *   launch.  A failed check returns a non-zero status and enqueues nothing.
