@@ -46,6 +46,28 @@ def test_cross_attention_cosmos_text_sampled(dl):
     compare(*gather_rows(O, L, rows), Or, Lr)
 
 
+@pytest.mark.parametrize("B,Nq,Nkv,kvl,H,D,density,rows", [
+    (1, 700, 300, 290, 2, 128, 0.3, 700),     # more queries than keys, ragged key tile
+    (2, 130, 2048, 2000, 2, 64, 0.05, 100),   # few queries over many keys, some rows unmasked
+    (1, 2048, 4200, 4100, 3, 128, 0.5, 2048), # one partial wave, split over key ranges by the default workspace
+])
+def test_general_mask_on_cross_attention(dl, B, Nq, Nkv, kvl, H, D, density, rows):
+    """A general mask with Nq != Nkv (video queries over a shorter or longer K/V):
+    bit j of row i allows key j, rows >= mask_rows attend every valid key."""
+    q, k, v, _ = wl.make_qkv(B, Nq, H, D, seed=Nq + 7 * Nkv, device=DEV, Nkv=Nkv)
+    g = torch.Generator().manual_seed(Nq + Nkv)
+    m = torch.rand((B, rows, kvl), generator=g) < density
+    m[:, 0] = False                                    # a row with no allowed key
+    bits = wl.pack_mask_bits(m).to(DEV)
+    O, L = dl.attn_fwd_masked(q, k, v, bits, mask_rows=rows, key_valid_len=kvl)
+    torch.cuda.synchronize()
+    allow = np.ones((B, Nq, kvl), dtype=bool)
+    allow[:, :rows] = m.numpy()
+    Or, Lr = oracle.attn(host_bits(q), host_bits(k), host_bits(v), key_valid_len=kvl, allow=allow)
+    compare(*_full(O, L), Or.transpose(0, 2, 1, 3), Lr)
+    assert torch.all(O[:, 0] == 0) and torch.all(torch.isneginf(L[:, :, 0]))
+
+
 def _masked_case(dl, B, T, Tp, H, D, density, seed, mask_rows=None, out_dtype=torch.float32, empty_rows=()):
     q, k, v, _ = wl.make_qkv(B, Tp, H, D, seed=seed, device=DEV)
     g = torch.Generator().manual_seed(seed)
