@@ -304,7 +304,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 8) {
         regs_decrease<kOtherRegs>();
         // ------------------------------------------------------------- MMA issuer
-        if (lane == 0 && n_tiles > 0) {
+        // The whole warp runs this block and one elected lane issues each
+        // product and commit (the *_warp forms), so the issue loop stays
+        // warp-uniform and keeps pace with the tensor pipe while the softmax
+        // warps keep every SM sub-partition's issue slots busy.
+        if (n_tiles > 0) {
             constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false);
             constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, true);
             const uint32_t tS0 = tmem, tS1 = tmem + 128;
@@ -312,35 +316,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // S_t = Q_t K^T : A = Q (K-major), B = K (K-major), K-dim = D.
             auto issue_qk = [&](uint32_t tS, uint32_t q_addr, uint32_t k_addr) {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-                    umma_ss(tS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                            kIdescQK, kk > 0 ? 1u : 0u);
-                }
+                const uint64_t dq = sdesc_sw128(q_addr, 16, 1024), dk = sdesc_sw128(k_addr, 16, 1024);
+                static_for<D / 16>([&](auto kk) {
+                    constexpr uint32_t off = (kk.value >> 2) * C::kBlockBytes + (kk.value & 3) * 32;
+                    umma_ss_warp<off>(tS, dq, dk, kIdescQK, kk.value > 0 ? 1u : 0u);
+                });
             };
             // O_t (+)= P_t V : A = P (TMEM, bf16 pairs), B = V (MN-major), K-dim = 128 keys.
             auto issue_pv = [&](uint32_t tO, uint32_t tP, uint32_t v_addr, bool accumulate) {
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    umma_ts(tO, tP + kk * 8, sdesc_sw128(v_addr + kk * 16 * 128, C::kBlockBytes, 1024), kIdescPV,
-                            (accumulate || kk > 0) ? 1u : 0u);
+                const uint64_t dv = sdesc_sw128(v_addr, C::kBlockBytes, 1024);
+                static_for<kBN / 16>([&](auto kk) {
+                    umma_ts_warp<kk.value * 16 * 128>(tO, tP + kk.value * 8, dv, kIdescPV,
+                                                      (accumulate || kk.value > 0) ? 1u : 0u);
+                });
             };
 
-            bool ok = wait_bounded(bar(C::kQFull + 0), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
-                      wait_bounded(bar(C::kQFull + 1), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
-                      wait_bounded(bar(C::kKVFull + 0), 0, wd, ROLE_MMA, SITE_KV_FULL);
+            bool ok = wait_bounded_warp(bar(C::kQFull + 0), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
+                      wait_bounded_warp(bar(C::kQFull + 1), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
+                      wait_bounded_warp(bar(C::kKVFull + 0), 0, wd, ROLE_MMA, SITE_KV_FULL);
             // S_0 number n is ready (the debug library can withhold one signal)
             auto commit_s0 = [&](int n) {
-                if (!inject(a, FAULT_SKIP_S_COMMIT, n)) umma_commit(bar(C::kSFull + 0));
+                if (!inject(a, FAULT_SKIP_S_COMMIT, n)) umma_commit_warp(bar(C::kSFull + 0));
             };
             if (ok) {
                 tc_fence_after();
                 issue_qk(tS0, sQ, sRing);
                 commit_s0(0);
                 issue_qk(tS1, sQ + TILE, sRing);
-                umma_commit(bar(C::kSFull + 1));
-                umma_commit(bar(C::kKVEmpty + 0));
+                umma_commit_warp(bar(C::kSFull + 1));
+                umma_commit_warp(bar(C::kKVEmpty + 0));
             }
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int iv = 2 * j + 1, ik = 2 * j + 2;
@@ -352,38 +356,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    k_addr + TILE <= sRing + S * TILE,
                                a.status, ROLE_MMA, BND_SMEM))
                     break;
-                ok = wait_bounded(bar(C::kKVFull + iv % S), static_cast<uint32_t>(iv / S) & 1u, wd, ROLE_MMA,
-                                  SITE_KV_FULL) &&
-                     wait_bounded(bar(C::kPFull + 0), ph, wd, ROLE_MMA, SITE_P_FULL);
+                ok = wait_bounded_warp(bar(C::kKVFull + iv % S), static_cast<uint32_t>(iv / S) & 1u, wd, ROLE_MMA,
+                                       SITE_KV_FULL) &&
+                     wait_bounded_warp(bar(C::kPFull + 0), ph, wd, ROLE_MMA, SITE_P_FULL);
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(tO0, tS0, v_addr, j > 0);
                 if (more) {
-                    ok = wait_bounded(bar(C::kKVFull + ik % S), static_cast<uint32_t>(ik / S) & 1u, wd, ROLE_MMA,
-                                      SITE_KV_FULL);
+                    ok = wait_bounded_warp(bar(C::kKVFull + ik % S), static_cast<uint32_t>(ik / S) & 1u, wd,
+                                           ROLE_MMA, SITE_KV_FULL);
                     if (!ok) break;
                     tc_fence_after();
                     issue_qk(tS0, sQ, k_addr);
                     commit_s0(j + 1);
                 } else {
-                    umma_commit(bar(C::kOFinal + 0));
+                    umma_commit_warp(bar(C::kOFinal + 0));
                 }
-                ok = wait_bounded(bar(C::kPFull + 1), ph, wd, ROLE_MMA, SITE_P_FULL);
+                ok = wait_bounded_warp(bar(C::kPFull + 1), ph, wd, ROLE_MMA, SITE_P_FULL);
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(tO1, tS1, v_addr, j > 0);
-                umma_commit(bar(C::kKVEmpty + iv % S));
+                umma_commit_warp(bar(C::kKVEmpty + iv % S));
                 if (more) {
                     issue_qk(tS1, sQ + TILE, k_addr);
-                    umma_commit(bar(C::kSFull + 1));
-                    umma_commit(bar(C::kKVEmpty + ik % S));
+                    umma_commit_warp(bar(C::kSFull + 1));
+                    umma_commit_warp(bar(C::kKVEmpty + ik % S));
                 } else {
-                    umma_commit(bar(C::kOFinal + 1));
+                    umma_commit_warp(bar(C::kOFinal + 1));
                 }
             }
             // Every product issued must finish before TMEM is released.
-            umma_commit(bar(C::kDrain));
-            wait_bounded(bar(C::kDrain), 0, wd_drain, ROLE_MMA, SITE_DRAIN);
+            umma_commit_warp(bar(C::kDrain));
+            wait_bounded_warp(bar(C::kDrain), 0, wd_drain, ROLE_MMA, SITE_DRAIN);
         }
         __syncwarp();
     } else {

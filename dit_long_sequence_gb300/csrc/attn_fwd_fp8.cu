@@ -198,7 +198,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 8) {
         regs_decrease<kOtherRegs>();
         // ------------------------------------------------------------- MMA issuer
-        if (lane == 0 && n_tiles > 0) {
+        // The whole warp runs this block and one elected lane issues each
+        // product and commit (the *_warp forms): the issue loop stays
+        // warp-uniform and keeps pace with the tensor pipe while the softmax
+        // warps keep every SM sub-partition's issue slots busy.
+        if (n_tiles > 0) {
             constexpr uint32_t kIdescQK = idesc_e4m3_f32(kBM, kBN, false);
             constexpr uint32_t kIdescPV = idesc_e4m3_f32(kBM, kD, true);
             const uint32_t tS0 = tmem, tS1 = tmem + 128;
@@ -206,34 +210,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // S_t = Q_t K^T: both K-major, 32 channels (32 bytes) per instruction.
             auto issue_qk = [&](uint32_t tS, uint32_t q_addr, uint32_t k_addr) {
-#pragma unroll
-                for (int kk = 0; kk < kD / 32; ++kk)
-                    umma_ss_f8(tS, sdesc_sw128(q_addr + kk * 32, 16, 1024), sdesc_sw128(k_addr + kk * 32, 16, 1024),
-                               kIdescQK, kk > 0 ? 1u : 0u);
+                const uint64_t dq = sdesc_sw128(q_addr, 16, 1024), dk = sdesc_sw128(k_addr, 16, 1024);
+                static_for<kD / 32>([&](auto kk) {
+                    umma_ss_f8_warp<kk.value * 32>(tS, dq, dk, kIdescQK, kk.value > 0 ? 1u : 0u);
+                });
             };
             // O_t (+)= P_t V: P from TMEM (8 columns = 32 keys per instruction),
             // V MN-major, 32 keys = four 8-row swizzle atoms = 4096 bytes.
             auto issue_pv = [&](uint32_t tO, uint32_t tP, uint32_t v_addr, bool accumulate) {
-#pragma unroll
-                for (int kk = 0; kk < kBN / 32; ++kk)
-                    umma_ts_f8(tO, tP + kk * 8, sdesc_sw128(v_addr + kk * 4096, 16384, 1024), kIdescPV,
-                               (accumulate || kk > 0) ? 1u : 0u);
+                const uint64_t dv = sdesc_sw128(v_addr, 16384, 1024);
+                static_for<kBN / 32>([&](auto kk) {
+                    umma_ts_f8_warp<kk.value * 4096>(tO, tP + kk.value * 8, dv, kIdescPV,
+                                                     (accumulate || kk.value > 0) ? 1u : 0u);
+                });
             };
 
-            bool ok = wait_bounded(bar(kQFull + 0), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
-                      wait_bounded(bar(kQFull + 1), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
-                      wait_bounded(bar(kKVFull + 0), 0, wd, ROLE_MMA, SITE_KV_FULL);
+            bool ok = wait_bounded_warp(bar(kQFull + 0), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
+                      wait_bounded_warp(bar(kQFull + 1), 0, wd, ROLE_MMA, SITE_Q_FULL) &&
+                      wait_bounded_warp(bar(kKVFull + 0), 0, wd, ROLE_MMA, SITE_KV_FULL);
             // S_0 number n is ready (the debug library can withhold one signal)
             auto commit_s0 = [&](int n) {
-                if (!inject(a, FAULT_SKIP_S_COMMIT, n)) umma_commit(bar(kSFull + 0));
+                if (!inject(a, FAULT_SKIP_S_COMMIT, n)) umma_commit_warp(bar(kSFull + 0));
             };
             if (ok) {
                 tc_fence_after();
                 issue_qk(tS0, sQ, sRing);
                 commit_s0(0);
                 issue_qk(tS1, sQ + kTile, sRing);
-                umma_commit(bar(kSFull + 1));
-                umma_commit(bar(kKVEmpty + 0));
+                umma_commit_warp(bar(kSFull + 1));
+                umma_commit_warp(bar(kKVEmpty + 0));
             }
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int iv = 2 * j + 1, ik = 2 * j + 2;
@@ -245,37 +250,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    k_addr + kTile <= sRing + S * kTile,
                                a.status, ROLE_MMA, BND_SMEM))
                     break;
-                ok = wait_bounded(bar(kKVFull + iv % S), static_cast<uint32_t>(iv / S) & 1u, wd, ROLE_MMA,
-                                  SITE_KV_FULL) &&
-                     wait_bounded(bar(kPFull + 0), ph, wd, ROLE_MMA, SITE_P_FULL);
+                ok = wait_bounded_warp(bar(kKVFull + iv % S), static_cast<uint32_t>(iv / S) & 1u, wd, ROLE_MMA,
+                                       SITE_KV_FULL) &&
+                     wait_bounded_warp(bar(kPFull + 0), ph, wd, ROLE_MMA, SITE_P_FULL);
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(tO0, tS0, v_addr, j > 0);
                 if (more) {
-                    ok = wait_bounded(bar(kKVFull + ik % S), static_cast<uint32_t>(ik / S) & 1u, wd, ROLE_MMA,
-                                      SITE_KV_FULL);
+                    ok = wait_bounded_warp(bar(kKVFull + ik % S), static_cast<uint32_t>(ik / S) & 1u, wd,
+                                           ROLE_MMA, SITE_KV_FULL);
                     if (!ok) break;
                     tc_fence_after();
                     issue_qk(tS0, sQ, k_addr);
                     commit_s0(j + 1);
                 } else {
-                    umma_commit(bar(kOFinal + 0));
+                    umma_commit_warp(bar(kOFinal + 0));
                 }
-                ok = wait_bounded(bar(kPFull + 1), ph, wd, ROLE_MMA, SITE_P_FULL);
+                ok = wait_bounded_warp(bar(kPFull + 1), ph, wd, ROLE_MMA, SITE_P_FULL);
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(tO1, tS1, v_addr, j > 0);
-                umma_commit(bar(kKVEmpty + iv % S));
+                umma_commit_warp(bar(kKVEmpty + iv % S));
                 if (more) {
                     issue_qk(tS1, sQ + kTile, k_addr);
-                    umma_commit(bar(kSFull + 1));
-                    umma_commit(bar(kKVEmpty + ik % S));
+                    umma_commit_warp(bar(kSFull + 1));
+                    umma_commit_warp(bar(kKVEmpty + ik % S));
                 } else {
-                    umma_commit(bar(kOFinal + 1));
+                    umma_commit_warp(bar(kOFinal + 1));
                 }
             }
-            umma_commit(bar(kDrain));
-            wait_bounded(bar(kDrain), 0, wd_drain, ROLE_MMA, SITE_DRAIN);
+            umma_commit_warp(bar(kDrain));
+            wait_bounded_warp(bar(kDrain), 0, wd_drain, ROLE_MMA, SITE_DRAIN);
         }
         __syncwarp();
     } else {

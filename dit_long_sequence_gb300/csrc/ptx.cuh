@@ -9,8 +9,21 @@
 
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <type_traits>
+#include <utility>
 
 namespace dit {
+
+// f(std::integral_constant<int, i>{}) for i = 0 .. N-1, each i a compile-time
+// constant (template arguments of the product statements below).
+template <int N, typename F, int... I>
+__device__ __forceinline__ void static_for_impl(F&& f, std::integer_sequence<int, I...>) {
+    (f(std::integral_constant<int, I>{}), ...);
+}
+template <int N, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+    static_for_impl<N>(f, std::make_integer_sequence<int, N>{});
+}
 
 // ------------------------------------------------------------------ basics
 
@@ -171,53 +184,97 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
            (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T   (one elected thread issues)
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
+// ------------------------------------------- products issued by a whole warp
+//
+// The forms below are executed by all 32 lanes of a converged warp, and
+// elect.sync picks the one lane that issues (the same lane every time in a
+// converged warp, so its products and commits keep their issue order).  The
+// code around them -- waits, loop control, descriptor arithmetic -- then runs
+// warp-uniform.  Measured on this GPU with eight softmax-like warps busy on
+// the same SM, a single-lane issuer (`if (lane == 0)`) issued one M128 N128
+// K16 product per 90-94 cycles; the warp-wide form kept the tensor pipe's own
+// rate, one per 64 cycles.
+
+// `OFF` is the operand's byte offset from the descriptor(s) passed in (a K
+// step within a tile): it is added inside the statement, so the compiler
+// keeps one base descriptor per tile live instead of hoisting every step's.
+// The start address is the descriptor's low field (address >> 4, 14 bits) and
+// shared-memory addresses stay below 2^18 bytes, so the add never carries
+// into the next field.
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 operands (K = 16 per instruction).
+template <uint32_t OFF>
+__device__ __forceinline__ void umma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 ad, bd;\n\t"
+        "add.s64 ad, %1, %5;\n\t"
+        "add.s64 bd, %2, %5;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(OFF >> 4)
         : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem], bf16 operands (offset applies to B).
+template <uint32_t OFF>
+__device__ __forceinline__ void umma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 bd;\n\t"
+        "add.s64 bd, %2, %5;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(OFF >> 4)
         : "memory");
 }
 
-// FP8 forms of the two products above (K = 32 per instruction).
-__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
+// FP8 forms of the two products above (E4M3, K = 32 per instruction).
+template <uint32_t OFF>
+__device__ __forceinline__ void umma_ss_f8_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 ad, bd;\n\t"
+        "add.s64 ad, %1, %5;\n\t"
+        "add.s64 bd, %2, %5;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(OFF >> 4)
         : "memory");
 }
 
-__device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
+template <uint32_t OFF>
+__device__ __forceinline__ void umma_ts_f8_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 bd;\n\t"
+        "add.s64 bd, %2, %5;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], bd, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(OFF >> 4)
         : "memory");
 }
 
-// Arrive on `bar` once every tcgen05 op issued so far by this thread is done.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
+// Arrive on `bar` once every tcgen05 op issued so far by the elected lane is
+// done.
+__device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
+// wait_bounded for a whole warp: every lane waits, and the result is the same
+// in all lanes (a lane that gave up makes the warp give up), so the warp stays
+// converged for the warp-wide forms above.
+__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity, Watchdog w, uint32_t role,
+                                                  uint32_t site) {
+    return __all_sync(0xffffffffu, wait_bounded(bar, parity, w, role, site));
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t gets lane (base+t).
