@@ -15,7 +15,8 @@
 // 12 warps:
 //   warps 0-3  softmax for query tile 0 (one TMEM lane = one row per thread)
 //   warps 4-7  softmax for query tile 1
-//   warp  8    tcgen05.mma issuer (one thread); owns the TMEM allocation
+//   warp  8    tcgen05.mma issuer (the whole warp runs the issue loop, one
+//              elected lane issues); owns the TMEM allocation
 //   warp  9    TMA producer (one thread): Q once, then K_0, V_0, K_1, V_1, ...
 //              through a ring of STAGES shared-memory slots
 //   warps 10-11 idle (they complete the third warpgroup)
@@ -26,10 +27,10 @@
 // P_t (bf16, 64 columns) is written by the softmax warps over the first half of
 // S_t and fed to the PV product as the TMEM A operand.
 //
-// Per KV tile j the MMA thread issues, in order,
+// Per KV tile j the MMA warp issues, in order,
 //   PV0(j) and QK0(j+1) once P0(j) is ready, then PV1(j) and QK1(j+1) once
 //   P1(j) is ready -- so the tensor pipe runs one tile's products while the
-//   other tile's softmax runs.  Products issued by one thread execute in order,
+//   other tile's softmax runs.  Products issued by one lane execute in order,
 //   which makes writing S_t(j+1) over P_t(j) safe after PV_t(j).
 //
 // Online softmax in log2 units with a lazy rescale: the running max m of a row
@@ -69,7 +70,7 @@
 // while m stays -inf), and a row with no allowed key at all ends with O = 0,
 // LSE = -inf.  With an occupancy map (one bit per (256-row block, key tile):
 // does any row of the block attend any key of the tile), every role walks only
-// the occupied key tiles -- the TMA producer loads, the MMA thread multiplies
+// the occupied key tiles -- the TMA producer loads, the MMA warp multiplies
 // and the softmax warps exponentiate nothing else.  The masked kernel splits
 // its last partial wave the same way: a piece walks the occupied tiles of its
 // own key range, and a piece whose range holds no key a row may attend gives

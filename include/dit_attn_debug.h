@@ -41,7 +41,7 @@ typedef enum {
     DIT_FAULT_SKIP_LOAD = 1,      /* the TMA thread skips K/V load `index` (K_j is
                                      load 2j, V_j load 2j+1 of the CTA's key
                                      tiles): no arrive, no copy               */
-    DIT_FAULT_SKIP_S_COMMIT = 2,  /* the MMA thread skips the completion signal
+    DIT_FAULT_SKIP_S_COMMIT = 2,  /* the MMA warp skips the completion signal
                                      of S for query tile 0, key tile `index`  */
     DIT_FAULT_SKIP_P_ARRIVE = 3   /* softmax warp 0 (query tile 0) skips its
                                      "P ready" arrive at key tile `index`     */
