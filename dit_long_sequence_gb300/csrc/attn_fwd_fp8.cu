@@ -250,17 +250,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    k_addr + kTile <= sRing + S * kTile,
                                a.status, ROLE_MMA, BND_SMEM))
                     break;
+                // K of the next tile as well as V of this one: both land long before P_0
+                // is ready, and waiting for them here keeps the K wait out of the chain
+                // that P_0 starts (P.V_0 -> Q.K_0 -> S_0 -> the softmax).
                 ok = wait_bounded_warp(bar(kKVFull + iv % S), static_cast<uint32_t>(iv / S) & 1u, wd, ROLE_MMA,
                                        SITE_KV_FULL) &&
+                     (!more || wait_bounded_warp(bar(kKVFull + ik % S), static_cast<uint32_t>(ik / S) & 1u, wd,
+                                                 ROLE_MMA, SITE_KV_FULL)) &&
                      wait_bounded_warp(bar(kPFull + 0), ph, wd, ROLE_MMA, SITE_P_FULL);
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(tO0, tS0, v_addr, j > 0);
                 if (more) {
-                    ok = wait_bounded_warp(bar(kKVFull + ik % S), static_cast<uint32_t>(ik / S) & 1u, wd,
-                                           ROLE_MMA, SITE_KV_FULL);
-                    if (!ok) break;
-                    tc_fence_after();
                     issue_qk(tS0, sQ, k_addr);
                     commit_s0(j + 1);
                 } else {
